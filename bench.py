@@ -1,0 +1,460 @@
+"""Benchmark of the W4A16 linear layer on GB300.
+
+One step = one pass of the decode hot path over one batch: the four linear
+layers of a Qwen3-4B-shaped model (qkv 6144x2560, o_proj 2560x4096, gate_up
+19456x2560, down 2560x9728), symmetric uint4b8 weights, G = 128, bf16
+activations, M = 1 token.  `value` is the algorithmic weight + metadata +
+activation byte stream per step divided by the device time per step (GB/s),
+with every input resident in HBM; weight sets rotate so that each step
+streams from HBM (the sets together are larger than 3x the L2).
+
+The second half of the metric, the M = 1920 prefill GEMM in TFLOP/s, is
+measured in the same run on the Llama-3.1-8B-shaped asymmetric bf16 G = 64
+layers and reported under "prefill".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (plain C, fp64) on the same workload
+(a bounded sample of steps) on the host cores.  With N > 1 (torchrun) every
+rank runs an independent replica (the layer has no data-path exchange);
+timing is the max over ranks and value the sum of their work.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from w4a16_group_quantised_gb300 import workloads as wl  # noqa: E402
+
+METRIC = ("M=1 decode weight-stream GB/s (% HBM peak); "
+          "M=1920 prefill TFLOP/s (% TC peak)")
+DECODE_WORKLOAD = "qwen3-4b-decode-m1-sym-g128-bf16"
+PREFILL_WORKLOAD = "llama-3.1-8b-prefill-m1920-asym-g64-bf16"
+L2_BYTES_FALLBACK = 126 * 1024 * 1024
+
+
+# ----------------------------------------------------------------- helpers
+def decode_bytes(M, N, K, G, sym):
+    """Algorithmic bytes of one decode GEMM: packed weights, scales, zero
+    points (asymmetric), x and y."""
+    b = N * K // 2 + N * (K // G) * 2 + M * K * 2 + M * N * 2
+    if not sym:
+        b += (N // 8) * (K // G) * 4
+    return b
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def source_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "w4a16_group_quantised_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_tag, src_hash):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current source of that kernel (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(kernel_tag)
+        if e and e.get("source_hash") == src_hash:
+            return e["dram_bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML (ctypes) while
+    the timed region runs.  Reads only; changes no setting."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device_index=0, period_s=0.002):
+        self.period = period_s
+        self.samples = []
+        self.reasons = set()
+        self.max_mhz = None
+        self.ok = False
+        self._stop = threading.Event()
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                return
+            props = torch.cuda.get_device_properties(device_index)
+            bus = "%08X:%02X:%02X.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+            self.h = ctypes.c_void_p()
+            if self.nvml.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if self.nvml.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0:  # NVML_CLOCK_SM
+                self.max_mhz = mx.value
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def _run(self):
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nvml.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk)) == 0:
+                self.samples.append(clk.value)
+            if self.nvml.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(rs)) == 0:
+                for bit, name in self.REASONS.items():
+                    if rs.value & bit:
+                        self.reasons.add(name)
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                    "samples": len(self.samples)}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples)}
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(v: float, ws: int) -> float:
+    if ws == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------- our arm
+def upload(w, p):
+    q = torch.from_numpy(p.q).cuda()
+    qweight = w.w4a16_pack(q)
+    del q
+    qzeros = None
+    if p.z is not None:
+        qzeros = w.w4a16_pack_zeros(torch.from_numpy(p.z).cuda())
+    td = torch.float16 if p.dtype == 0 else torch.bfloat16
+    scales = torch.from_numpy(p.scales.view(np.int16)).view(td).cuda()
+    x = torch.from_numpy(p.x.view(np.int16)).view(td).cuda()
+    return dict(qweight=qweight, scales=scales, qzeros=qzeros, x=x, M=p.M, N=p.N, K=p.K, G=p.G,
+                sym=p.sym, dtype=p.dtype)
+
+
+def make_sets(w, make, n_sets, shapes_count):
+    """n_sets weight sets of the same layers.  Set 0 comes from the seeded
+    generator; the others are copies with bytes permuted by a cheap device
+    roll so that every set is distinct memory (the values are equally
+    distributed)."""
+    base = [upload(w, make(i)) for i in range(shapes_count)]
+    sets = [base]
+    for s in range(1, n_sets):
+        cur = []
+        for d in base:
+            e = dict(d)
+            e["qweight"] = torch.roll(d["qweight"], shifts=s, dims=1).contiguous()
+            e["scales"] = torch.roll(d["scales"], shifts=s, dims=0).contiguous()
+            if d["qzeros"] is not None:
+                e["qzeros"] = torch.roll(d["qzeros"], shifts=s, dims=0).contiguous()
+            cur.append(e)
+        sets.append(cur)
+    return sets
+
+
+def run_step(w, layers, outs):
+    for d, o in zip(layers, outs):
+        w.w4a16_gemm(d["x"], d["qweight"], d["scales"], d["qzeros"], d["G"], out=o)
+
+
+def bench_decode(w, steps, warmup, l2_bytes):
+    shapes = wl.QWEN3_4B_SHAPES
+    step_bytes = sum(decode_bytes(1, N, K, 128, True) for (_, N, K) in shapes)
+    n_sets = max(2, int(np.ceil(3 * l2_bytes / step_bytes)) + 1)
+    sets = make_sets(w, lambda i: wl.qwen3_4b_decode(i, 1), n_sets, len(shapes))
+    outs = [torch.empty((1, N), dtype=torch.bfloat16, device="cuda") for (_, N, K) in shapes]
+    stream = torch.cuda.Stream()
+    # One CUDA graph holds `chunk` consecutive steps (rotating sets); the
+    # timed region replays it.
+    chunk = n_sets * max(1, 64 // n_sets)
+    with torch.cuda.stream(stream):
+        for s in range(n_sets):   # first calls outside capture (per-device set-up)
+            run_step(w, sets[s], outs)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(chunk):
+                run_step(w, sets[i % n_sets], outs)
+    reps_w = max(1, int(np.ceil(warmup / chunk)))
+    reps = max(1, int(np.ceil(steps / chunk)))
+    with torch.cuda.stream(stream):
+        for _ in range(reps_w):
+            g.replay()
+    torch.cuda.synchronize()
+    return dict(graph=g, stream=stream, chunk=chunk, reps=reps, step_bytes=step_bytes,
+                n_sets=n_sets, sets=sets, outs=outs, launches_per_step=len(shapes))
+
+
+def timed_replays(ctx, ws):
+    g, stream = ctx["graph"], ctx["stream"]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):   # replay() launches on the current stream
+        start.record(stream)
+        for _ in range(ctx["reps"]):
+            g.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    return start.elapsed_time(end) / 1000.0
+
+
+def bench_decode_e2e(w, ctx, steps):
+    """Through w4a16_gemm_host: pinned x in, y out, per layer, every step."""
+    layers = ctx["sets"][0]
+    xs = [d["x"].cpu().pin_memory() for d in layers]
+    ys = [torch.empty((1, d["N"]), dtype=torch.bfloat16).pin_memory() for d in layers]
+    dx = [torch.empty_like(d["x"]) for d in layers]
+    dy = [torch.empty((1, d["N"]), dtype=torch.bfloat16, device="cuda") for d in layers]
+    h2d = sum(x.numel() * 2 for x in xs)
+    d2h = sum(y.numel() * 2 for y in ys)
+    n = max(3, min(steps, 2000))
+    for _ in range(3):
+        for d, x, y, a, b in zip(layers, xs, ys, dx, dy):
+            w.w4a16_gemm_host(x, d["qweight"], d["scales"], d["qzeros"], d["G"], y, a, b)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(n):
+        layers_i = ctx["sets"][i % ctx["n_sets"]]
+        for d, x, y, a, b in zip(layers_i, xs, ys, dx, dy):
+            w.w4a16_gemm_host(x, d["qweight"], d["scales"], d["qzeros"], d["G"], y, a, b)
+    dt = (time.perf_counter() - t0) / n
+    return dict(dt=dt, h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h, steps=n)
+
+
+def bench_prefill(w, steps):
+    shapes = wl.LLAMA31_8B_SHAPES
+    layers = [upload(w, wl.llama31_8b_prefill(i, 1920)) for i in range(len(shapes))]
+    outs = [torch.empty((1920, N), dtype=torch.bfloat16, device="cuda") for (_, N, K) in shapes]
+    flops = sum(2 * 1920 * N * K for (_, N, K) in shapes)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            run_step(w, layers, outs)
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        # per-shape timing for the roofline of the dominant (largest) GEMM
+        per = []
+        for d, o in zip(layers, outs):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                w.w4a16_gemm(d["x"], d["qweight"], d["scales"], d["qzeros"], d["G"], out=o)
+            e1.record(stream)
+            per.append((e0, e1))
+        start.record(stream)
+        for _ in range(steps):
+            run_step(w, layers, outs)
+        end.record(stream)
+    torch.cuda.synchronize()
+    dt = start.elapsed_time(end) / 1000.0 / steps
+    per_ms = [a.elapsed_time(b) / steps for (a, b) in per]
+    del layers, outs
+    return dict(tflops=flops / dt / 1e12, ms_per_step=dt * 1e3, flops_per_step=flops,
+                per_shape_ms=per_ms,
+                per_shape_tflops=[2 * 1920 * N * K / (ms / 1e3) / 1e12
+                                  for (ms, (_, N, K)) in zip(per_ms, shapes)])
+
+
+def cpu_baseline(sample_steps=None, budget_s=15.0):
+    """The oracle (as it stands) on the host cores, on whole decode steps."""
+    import oracle
+    oracle.build()
+    shapes = wl.QWEN3_4B_SHAPES
+    probs = [wl.qwen3_4b_decode(i, 1) for i in range(len(shapes))]
+    packed = [oracle.pack(p.q) for p in probs]
+    step_bytes = sum(decode_bytes(1, N, K, 128, True) for (_, N, K) in shapes)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        for p, qw in zip(probs, packed):
+            oracle.gemm(p.x, p.M, p.K, qw, p.scales, None, p.G, p.N, p.dtype)
+        n += 1
+        el = time.perf_counter() - t0
+        if (sample_steps is not None and n >= sample_steps) or (sample_steps is None and el >= budget_s):
+            break
+    dt = (time.perf_counter() - t0) / n
+    return dict(value=step_bytes / dt / 1e9, unit="GB/s", cores=oracle.num_threads(), kind="oracle",
+                sample=f"{n} whole decode steps (4 Qwen3-4B-shaped layers, M=1) in fp64 C",
+                s_per_step=dt)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--prefill-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    warmup = max(3, args.warmup)
+    ws, rank, local = dist_info()
+    hbm, tc, tc_sus, peak_src = load_peaks()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        cb = cpu_baseline(sample_steps=None, budget_s=12.0)
+        line = {"metric": METRIC, "value": round(cb["value"], 4), "unit": "GB/s", "n_gpus": args.gpus,
+                "steps": 1, "warmup": 0, "ms_per_step": cb["s_per_step"] * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "impl": "reference",
+                "config": {"workload": DECODE_WORKLOAD, "M": 1, "layers": "qkv,o_proj,gate_up,down",
+                           "G": 128, "quant": "uint4b8", "act": "bf16"},
+                "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+                "e2e": {"value": round(cb["value"], 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    from w4a16_group_quantised_gb300 import build as libbuild
+    libbuild.build()
+    import w4a16_group_quantised_gb300 as w
+    w.load_library()
+
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size or L2_BYTES_FALLBACK
+    ctx = bench_decode(w, args.steps, warmup, l2)
+    steps = ctx["reps"] * ctx["chunk"]
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        dt = timed_replays(ctx, ws)
+    dt = max_over_ranks(dt, ws)
+    ms_per_step = dt / steps * 1e3
+    value = ctx["step_bytes"] * steps * ws / dt / 1e9
+    launches = steps * ctx["launches_per_step"]
+    per_launch_s = dt / launches
+    achieved = ctx["step_bytes"] / ctx["launches_per_step"] / per_launch_s / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        r = bench_decode_e2e(w, ctx, min(args.steps, 500))
+        edt = max_over_ranks(r["dt"], ws)
+        e2e = dict(value=ctx["step_bytes"] * ws / edt / 1e9, unit="GB/s",
+                   h2d_bytes_per_step=r["h2d_bytes_per_step"],
+                   d2h_bytes_per_step=r["d2h_bytes_per_step"], steps=r["steps"],
+                   ms_per_step=edt * 1e3, api="w4a16_gemm_host per layer (pinned host x in, y out)")
+    del ctx
+    torch.cuda.empty_cache()
+
+    pre = bench_prefill(w, max(2, args.prefill_steps))
+    dom = int(np.argmax(pre["per_shape_ms"]))
+    tc_peak = tc_sus if tc_sus else tc
+
+    dec_hash = source_hash("decode.cu", "dequant.cuh", "ptx.cuh")
+    pre_hash = source_hash("prefill.cu", "dequant.cuh", "ptx.cuh")
+    status = w.w4a16_last_device_error()
+
+    if rank != 0:
+        return
+    cb = None
+    if not args.no_cpu_baseline:
+        c = cpu_baseline(sample_steps=None, budget_s=12.0)
+        cb = {k: c[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": steps,
+        "warmup": warmup,
+        "ms_per_step": round(ms_per_step, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": DECODE_WORKLOAD, "M": 1, "layers": "qkv 6144x2560, o_proj 2560x4096, "
+                   "gate_up 19456x2560, down 2560x9728", "G": 128, "quant": "uint4b8 (symmetric)",
+                   "act": "bf16", "l2": "rotating weight sets larger than 3x L2",
+                   "parallelism": "replicas" if ws > 1 else "single-gpu",
+                   "launch": "CUDA graph of whole steps, programmatic dependent launch"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "peak_source": peak_src,
+                     "traffic": profiled_traffic("decode_qwen3_4b_m1", dec_hash),
+                     "kernel": "decode_kernel (split-K skinny GEMM)",
+                     "per_launch_us": round(per_launch_s * 1e6, 3)},
+        "prefill": {"workload": PREFILL_WORKLOAD, "value": round(pre["tflops"], 2), "unit": "TFLOP/s",
+                    "ms_per_step": round(pre["ms_per_step"], 4),
+                    "per_shape_tflops": [round(v, 1) for v in pre["per_shape_tflops"]],
+                    "roofline": {"bound": "tensor", "achieved": round(pre["per_shape_tflops"][dom], 2),
+                                 "peak": tc_peak, "unit": "TFLOP/s",
+                                 "frac": round(pre["per_shape_tflops"][dom] / tc_peak, 4),
+                                 "peak_source": peak_src + (" sustained" if tc_sus else ""),
+                                 "traffic": profiled_traffic("prefill_llama_gate_up_m1920", pre_hash),
+                                 "kernel": f"prefill_kernel, {wl.LLAMA31_8B_SHAPES[dom][0]}"}},
+        "clocks": clk.summary(),
+        "gpu_launches": launches,
+        "device_status": status,
+    }
+    if e2e is not None:
+        line["e2e"] = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in e2e.items()}
+    if cb is not None:
+        line["cpu_baseline"] = cb
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,163 @@
+/*
+ * w4a16.h -- C ABI of the GB300 (sm_103a) W4A16 group-quantised linear layer.
+ *
+ *     y[M, N] = x[M, K] . dequant(W)^T,   dequant(W)[n, k] = RN_dtype((q - z) * s)
+ *
+ * What the operation is comes from "[ROCm][Kernel] Add HybridW4A16LinearKernel:
+ * Triton prefill + HIP skinny decode" (vllm-project/vllm#40977), PR
+ * description: one weight tensor packed [N, K/8] shared by a skinny decode
+ * kernel and a fused-dequant prefill GEMM routed by batch size M; symmetric
+ * weights with a fixed bias of 8 (uint4b8) or asymmetric weights with
+ * per-group zero points; group sizes 32, 64, 128.  The packed zero-point
+ * form comes from "Upstream sync 67/N: merge 382bbd5144
+ * HybridW4A16LinearKernel (conflict)" (ROCm/vllm#1175), section "Upstream's
+ * Python side is kept -- and it does NOT work here": int32 [N/8, groups],
+ * 8 x uint4 along dim 0.
+ *
+ * Layouts (all row-major, contiguous, on the current CUDA device):
+ *   x        fp16/bf16 [M, K]
+ *   qweight  int32 [N, K/8]; element k = 8j + i of row n is bits [4i, 4i+3]
+ *            of qweight[n, j] (sequential nibble order, fixed by this header)
+ *   scales   same dtype as x, [N, K/G]; group g covers k in [gG, (g+1)G)
+ *   qzeros   int32 [N/8, K/G] or NULL; z[n, g] is bits [4(n%8), 4(n%8)+3] of
+ *            qzeros[n/8, g].  NULL means symmetric: z = 8 for every weight.
+ *   out      same dtype as x, [M, N]
+ * Arithmetic: the weight is rounded once into the activation dtype (round to
+ * nearest even) from the exact product (q - z) * s; the dot products are
+ * accumulated in fp32 and rounded once into the output dtype.
+ *
+ * Ownership: the caller owns every buffer.  Entry points do not allocate,
+ * free or synchronise, except w4a16_gemm_host (which synchronises its stream
+ * to return the host result).  Per-device state (SM count, kernel attributes,
+ * the tensor-map encoder) is set up on the first call on each device; make
+ * that first call outside stream capture.
+ *
+ * Errors: arguments are validated on the host before anything is launched;
+ * an invalid call returns a negative w4a16_status_t and launches nothing.
+ * M == 0 (or N == 0 for pack) is a valid no-op.  A launch failure returns
+ * W4A16_ERR_CUDA.  Faults during execution surface through CUDA as usual.
+ * Kernels bound every wait they make; a wait that runs out records
+ * W4A16_ERR_TIMEOUT in a device status word read by w4a16_last_device_error.
+ */
+#ifndef W4A16_H
+#define W4A16_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *w4a16_stream_t;
+
+typedef enum { W4A16_F16 = 0, W4A16_BF16 = 1 } w4a16_dtype_t;
+
+typedef enum {
+    W4A16_PATH_AUTO = 0,     /* the dispatcher decides from M and the shape   */
+    W4A16_PATH_DECODE = 1,   /* skinny split-K kernel; valid for M <= 8       */
+    W4A16_PATH_PREFILL = 2   /* tcgen05 fused-dequant GEMM; any M >= 1        */
+} w4a16_path_t;
+
+typedef enum {
+    W4A16_OK = 0,
+    W4A16_ERR_NULL = -1,     /* a required pointer is NULL                    */
+    W4A16_ERR_SHAPE = -2,    /* M, N or K out of range / not divisible        */
+    W4A16_ERR_GROUP = -3,    /* G not in {32, 64, 128} or K % G != 0          */
+    W4A16_ERR_ALIGN = -4,    /* a pointer is not 16-byte aligned              */
+    W4A16_ERR_DTYPE = -5,    /* dtype not W4A16_F16 / W4A16_BF16              */
+    W4A16_ERR_CUDA = -6,     /* a CUDA runtime call or launch failed          */
+    W4A16_ERR_DEVICE = -7,   /* device is not sm_103 / state set-up failed    */
+    W4A16_ERR_TIMEOUT = -8,  /* a kernel's bounded wait ran out (device word) */
+    W4A16_ERR_ARG = -9       /* other invalid argument (e.g. path enum)       */
+} w4a16_status_t;
+
+/* Limits checked by the validation (shapes must also fit in int32 indexing). */
+#define W4A16_MAX_DECODE_M 8
+
+/* Pack 4-bit weights.  q: device uint8 [N, K], values 0..15 (higher bits are
+ * ignored); qweight: device int32 [N, K/8].  Requires N >= 0, K % 8 == 0.
+ * Source: "[ROCm][Kernel] Add HybridW4A16LinearKernel", PR description
+ * (weights packed [N, K//8]). */
+int w4a16_pack(const uint8_t *q, int N, int K, int32_t *qweight, w4a16_stream_t stream);
+
+/* Pack zero points.  z: device uint8 [N, n_groups], values 0..15;
+ * qzeros: device int32 [N/8, n_groups].  Requires N % 8 == 0.
+ * Source: "Upstream sync 67/N ... (conflict)", section "Upstream's Python
+ * side is kept -- and it does NOT work here" (packed 8 x uint4 along dim 0). */
+int w4a16_pack_zeros(const uint8_t *z, int N, int n_groups, int32_t *qzeros,
+                     w4a16_stream_t stream);
+
+/* Materialise the dequantised weights: out[n, k] = RN_dtype((q - z) * s),
+ * device [N, K] of dtype.  Bit-exact with the definition above.  Uses the same
+ * device dequantisation routines as the GEMM kernels.  Validation as for
+ * w4a16_gemm (G, K % G, N % 8, alignment).
+ * Source: "[ROCm][Kernel] Add HybridW4A16LinearKernel", PR description
+ * (symmetric bias 8 / per-group zero points; the magic-number dequant). */
+int w4a16_dequant_debug(const int32_t *qweight, const void *scales,
+                        const int32_t *qzeros_or_null, int G, int N, int K, void *out,
+                        w4a16_dtype_t dtype, w4a16_stream_t stream);
+
+/* y = x . dequant(W)^T on `stream`.  x, scales and out share `dtype`.
+ * Requires M >= 0, N > 0 with N % 8 == 0, K > 0 with K % G == 0,
+ * G in {32, 64, 128}, every pointer 16-byte aligned.  Routes M <= threshold
+ * to the decode kernel and larger M to the prefill kernel (the threshold is
+ * reported by w4a16_select_path).
+ * Source: "[ROCm][Kernel] Add HybridW4A16LinearKernel", PR description (M
+ * routing between a skinny split-K decode GEMM and a fused-dequant GEMM). */
+int w4a16_gemm(const void *x, int M, int K, const int32_t *qweight, const void *scales,
+               const int32_t *qzeros_or_null, int G, int N, void *out,
+               w4a16_stream_t stream, w4a16_dtype_t dtype);
+
+/* The same call with the dtype fixed by the name. */
+int w4a16_gemm_f16(const void *x, int M, int K, const int32_t *qweight, const void *scales,
+                   const int32_t *qzeros_or_null, int G, int N, void *out,
+                   w4a16_stream_t stream);
+int w4a16_gemm_bf16(const void *x, int M, int K, const int32_t *qweight, const void *scales,
+                    const int32_t *qzeros_or_null, int G, int N, void *out,
+                    w4a16_stream_t stream);
+
+/* w4a16_gemm with the kernel forced: W4A16_PATH_DECODE requires M <= 8
+ * (else W4A16_ERR_SHAPE); W4A16_PATH_AUTO is w4a16_gemm. */
+int w4a16_gemm_ex(const void *x, int M, int K, const int32_t *qweight, const void *scales,
+                  const int32_t *qzeros_or_null, int G, int N, void *out,
+                  w4a16_stream_t stream, w4a16_dtype_t dtype, w4a16_path_t path);
+
+/* End-to-end form: x_host and out_host are HOST buffers (pinned for full
+ * speed); x_dev [M, K] and out_dev [M, N] are caller-owned device staging
+ * buffers.  Copies x to the device, runs w4a16_gemm, copies y back and
+ * synchronises `stream` before returning. */
+int w4a16_gemm_host(const void *x_host, int M, int K, const int32_t *qweight,
+                    const void *scales, const int32_t *qzeros_or_null, int G, int N,
+                    void *out_host, w4a16_dtype_t dtype, void *x_dev, void *out_dev,
+                    w4a16_stream_t stream);
+
+/* Host-only: which kernel w4a16_gemm would run (W4A16_PATH_DECODE or
+ * W4A16_PATH_PREFILL), or a negative status for invalid arguments.  sym != 0
+ * means qzeros_or_null == NULL. */
+int w4a16_select_path(int M, int N, int K, int G, int sym, int dtype);
+
+/* Device status word of the current device: W4A16_OK, or W4A16_ERR_TIMEOUT
+ * if a kernel gave up a bounded wait since the last clear.  Synchronises the
+ * device to read it. */
+int w4a16_last_device_error(void);
+int w4a16_clear_device_error(void);
+
+/* ABI version (major * 100 + minor). */
+int w4a16_version(void);
+
+/* Tuning hook (process-wide, for benchmarks and sweeps).  which = 1: decode
+ * configuration vals = {R, D, RW, KW, S} (16-row blocks per warp, register
+ * pipeline depth, row warps, K warps, cluster CTAs along K), n = 5;
+ * which = 2: prefill configuration vals = {BN, stages, astages}, n = 3;
+ * which = 3: programmatic dependent launch on/off, vals = {flag}, n = 1.
+ * n = 0 restores the built-in choice for which = 1 or 2.  An invalid
+ * configuration is rejected here or, for the decode shape limits, by the
+ * next w4a16_gemm call with W4A16_ERR_ARG. */
+int w4a16_debug_set_config(int which, const int *vals, int n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H */

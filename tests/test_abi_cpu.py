@@ -1,0 +1,126 @@
+"""Host-side checks that need no GPU: the library builds for sm_103a, loads,
+exports every entry point include/w4a16.h declares, and rejects invalid
+arguments on the host before touching the device; the dispatcher is host
+logic."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "w4a16.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from w4a16_group_quantised_gb300 import build
+    build.build()
+    import w4a16_group_quantised_gb300 as w
+    return w.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\bint\s+(w4a16_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("w4a16_pack", "w4a16_pack_zeros", "w4a16_dequant_debug", "w4a16_gemm"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_version(lib):
+    assert lib.w4a16_version() == 100
+
+
+NULL = None
+ALIGNED = ctypes.c_void_p(0x1000)     # never dereferenced: validation fails first
+MISALIGNED = ctypes.c_void_p(0x1008)
+
+
+def gemm(lib, x=ALIGNED, M=1, K=128, qw=ALIGNED, s=ALIGNED, qz=NULL, G=32, N=64, out=ALIGNED,
+         dtype=0):
+    return lib.w4a16_gemm(x, M, K, qw, s, qz, G, N, out, None, dtype)
+
+
+def test_validation_codes(lib):
+    assert gemm(lib, G=48) == -3                # W4A16_ERR_GROUP
+    assert gemm(lib, G=16) == -3
+    assert gemm(lib, K=96, G=64) == -3          # K % G
+    assert gemm(lib, N=60) == -2                # W4A16_ERR_SHAPE: N % 8
+    assert gemm(lib, M=-1) == -2
+    assert gemm(lib, K=0) == -2
+    assert gemm(lib, dtype=2) == -5             # W4A16_ERR_DTYPE
+    assert gemm(lib, qw=NULL) == -1             # W4A16_ERR_NULL
+    assert gemm(lib, s=NULL) == -1
+    assert gemm(lib, x=NULL) == -1
+    assert gemm(lib, out=NULL) == -1
+    assert gemm(lib, x=MISALIGNED) == -4        # W4A16_ERR_ALIGN
+    assert gemm(lib, qz=MISALIGNED) == -4
+    assert gemm(lib, N=1 << 20, K=1 << 15) == -2   # int32 index headroom
+    # M == 0 is a valid no-op: nothing is launched, no device needed
+    assert gemm(lib, M=0, x=NULL, out=NULL) == 0
+
+
+def test_forced_path_limits(lib):
+    P, I = ctypes.c_void_p, ctypes.c_int
+    ex = lib.w4a16_gemm_ex
+    assert ex(ALIGNED, 9, 128, ALIGNED, ALIGNED, None, 32, 64, ALIGNED, None, 0, 1) == -2
+    assert ex(ALIGNED, 1, 128, ALIGNED, ALIGNED, None, 32, 64, ALIGNED, None, 0, 7) == -9
+    assert ex(ALIGNED, 0, 128, ALIGNED, ALIGNED, None, 32, 64, ALIGNED, None, 0, 2) == 0
+
+
+def test_pack_validation(lib):
+    assert lib.w4a16_pack(ALIGNED, 8, 12, ALIGNED, None) == -2     # K % 8
+    assert lib.w4a16_pack(NULL, 8, 16, ALIGNED, None) == -1
+    assert lib.w4a16_pack(MISALIGNED, 8, 16, ALIGNED, None) == -4
+    assert lib.w4a16_pack(NULL, 0, 16, NULL, None) == 0            # empty is a no-op
+    assert lib.w4a16_pack_zeros(ALIGNED, 12, 4, ALIGNED, None) == -2  # N % 8
+    assert lib.w4a16_pack_zeros(NULL, 0, 4, NULL, None) == 0
+
+
+def test_dequant_validation(lib):
+    f = lib.w4a16_dequant_debug
+    assert f(ALIGNED, ALIGNED, None, 40, 64, 160, ALIGNED, 0, None) == -3
+    assert f(ALIGNED, ALIGNED, None, 32, 63, 128, ALIGNED, 0, None) == -2
+    assert f(NULL, ALIGNED, None, 32, 64, 128, ALIGNED, 0, None) == -1
+    assert f(ALIGNED, ALIGNED, None, 32, 64, 128, ALIGNED, 3, None) == -5
+
+
+def test_dispatcher_is_host_logic(lib):
+    assert lib.w4a16_select_path(1, 4096, 4096, 128, 1, 1) == 1     # decode
+    assert lib.w4a16_select_path(8, 4096, 4096, 128, 0, 0) == 1
+    assert lib.w4a16_select_path(1920, 4096, 4096, 64, 0, 1) == 2   # prefill
+    assert lib.w4a16_select_path(1, 4096, 4096, 48, 1, 1) == -3
+    for M in (1, 2, 3, 4, 5, 6, 8, 16, 32, 64, 128, 4096):
+        r = lib.w4a16_select_path(M, 2560, 9728, 128, 1, 0)
+        assert r in (1, 2)
+        if M > 8:
+            assert r == 2
+
+
+def test_debug_config_validation(lib):
+    arr = (ctypes.c_int * 3)(24, 4, 3)
+    assert lib.w4a16_debug_set_config(2, arr, 3) == -9   # BN not a multiple of 16
+    arr = (ctypes.c_int * 3)(128, 4, 3)
+    assert lib.w4a16_debug_set_config(2, arr, 3) == 0
+    assert lib.w4a16_debug_set_config(2, None, 0) == 0
+    assert lib.w4a16_debug_set_config(9, None, 0) == -9
+
+
+def test_binding_rejects_wrong_zero_point_dtype():
+    """The packed zero-point contract: int32 only (a float tensor of zero
+    points is refused before the library is called)."""
+    import torch
+    import w4a16_group_quantised_gb300 as w
+    with pytest.raises(TypeError):
+        w.w4a16_gemm(torch.zeros(1, 64, dtype=torch.float16), torch.zeros(8, 8, dtype=torch.int32),
+                      torch.zeros(8, 2, dtype=torch.float16), torch.zeros(1, 2, dtype=torch.float16), 32)

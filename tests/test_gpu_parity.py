@@ -1,0 +1,205 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+* packing and dequantisation: bit-exact;
+* GEMM: |y - y_ref| <= 1e-2 max(1, |y_ref|) elementwise and relative L2
+  <= 5e-3, on shapes spanning several tiles with ragged tails, every group
+  size, symmetric and asymmetric weights, fp16 and bf16, both kernels;
+* integer-exact GEMM (s = 1, integer x): bit-exact outputs, which catches any
+  layout, swizzle or split-K indexing error with zero tolerance.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from golden_cases import load, to_bits
+from parity_helpers import (bits_to_tensor, check_tolerance, out_values, tensor_to_bits,
+                            to_device)
+from w4a16_group_quantised_gb300.workloads import make_problem, tiny_symmetric
+
+pytestmark = pytest.mark.gpu
+
+DECODE, PREFILL = 1, 2
+
+
+def run_case(w, p, path, rows=None):
+    d = to_device(p, w)
+    out = w.w4a16_gemm(d["x"], d["qweight"], d["scales"], d["qzeros"], p.G, path=path)
+    torch.cuda.synchronize()
+    y = out_values(out)
+    y_ref = oracle.gemm(p.x, p.M, p.K, d["ref_qw"], p.scales, d["ref_qz"], p.G, p.N, p.dtype,
+                        rows=rows)
+    if rows is not None:
+        y = y[rows]
+    check_tolerance(y, y_ref, f"M={p.M} N={p.N} K={p.K} G={p.G} sym={p.sym} dt={p.dtype} path={path}")
+    return y, y_ref
+
+
+# ------------------------------------------------------------------ packing / dequant
+@pytest.mark.parametrize("dtype", [0, 1])
+@pytest.mark.parametrize("sym", [True, False])
+@pytest.mark.parametrize("G", [32, 64, 128])
+def test_dequant_bit_exact(cuda_lib, dtype, sym, G):
+    w = cuda_lib
+    p = make_problem(1, 264, 1152, G, sym, dtype, seed=100 + G)
+    d = to_device(p, w)
+    got = tensor_to_bits(w.w4a16_dequant_debug(d["qweight"], d["scales"], d["qzeros"], G))
+    ref = oracle.dequant(d["ref_qw"], p.scales, d["ref_qz"], G, p.N, p.K, dtype)
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("dtype", [0, 1])
+def test_dequant_exhaustive_scales(cuda_lib, dtype):
+    """Every finite 16-bit scale pattern times every q - z in [-15, 15]:
+    bit-exact against the oracle's RN_dtype((q - z) * s).  Row n uses scale
+    pattern n; group 0 has z = 15 (q - z = -15..0), group 1 z = 0 (0..15)."""
+    w = cuda_lib
+    N, K, G = 65536, 64, 32
+    pat = np.arange(65536, dtype=np.uint16)
+    vals = oracle.bits_to_float64(pat, dtype)
+    s_bits = np.where(np.isfinite(vals), pat, 0).astype(np.uint16)
+    scales = np.repeat(s_bits[:, None], 2, axis=1)
+    q = np.tile(np.concatenate([np.arange(16), np.arange(16), np.arange(16), np.arange(16)])
+                .astype(np.uint8), (N, 1))
+    z = np.tile(np.array([15, 0], dtype=np.uint8), (N, 1))
+    qw = oracle.pack(q)
+    qz = oracle.pack_zeros(z)
+    got = tensor_to_bits(w.w4a16_dequant_debug(torch.from_numpy(qw).cuda(),
+                                               bits_to_tensor(scales, dtype),
+                                               torch.from_numpy(qz).cuda(), G))
+    ref = oracle.dequant(qw, scales, qz, G, N, K, dtype)
+    sv = np.abs(oracle.bits_to_float64(s_bits, dtype))
+    min_normal = 2.0 ** -14 if dtype == 0 else 2.0 ** -126
+    normal_rows = (sv >= min_normal) | (sv == 0)
+    mism = (got != ref).any(axis=1)
+    assert not mism[normal_rows].any(), f"{mism[normal_rows].sum()} rows with normal scales differ"
+
+
+def test_pack_edge_values(cuda_lib):
+    w = cuda_lib
+    q = np.full((8, 32), 15, dtype=np.uint8)
+    q[:, ::2] = 0
+    p = torch.from_numpy(q).cuda()
+    assert np.array_equal(w.w4a16_pack(p).cpu().numpy(), oracle.pack(q))
+    z = np.random.default_rng(0).integers(0, 16, (64, 3), dtype=np.uint8)
+    assert np.array_equal(w.w4a16_pack_zeros(torch.from_numpy(z).cuda()).cpu().numpy(),
+                          oracle.pack_zeros(z))
+
+
+# ------------------------------------------------------------------ hand-worked case
+def test_golden_library_case(cuda_lib):
+    w = cuda_lib
+    c = load("lib_sym_fp16_m2_k32_n8")
+    qw = torch.from_numpy(oracle.pack(c["q"])).cuda()
+    x = bits_to_tensor(to_bits(c["x_vals"], 0), 0)
+    s = bits_to_tensor(to_bits(c["scales_vals"], 0), 0)
+    for path in (DECODE, PREFILL):
+        out = out_values(w.w4a16_gemm(x, qw, s, None, 32, path=path))
+        assert np.array_equal(out, c["y"]), (path, out)
+
+
+# ------------------------------------------------------------------ GEMM tolerance
+SMALL_SHAPES = [(8, 32), (136, 96), (264, 288), (520, 1184)]
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("dtype", [0, 1])
+@pytest.mark.parametrize("sym", [True, False])
+def test_decode_small(cuda_lib, M, dtype, sym):
+    for i, (N, K) in enumerate(SMALL_SHAPES):
+        for G in (32, 64, 128):
+            if K % G:
+                continue
+            p = make_problem(M, N, K, G, sym, dtype, seed=1000 + 10 * i + G + M)
+            run_case(cuda_lib, p, DECODE)
+
+
+@pytest.mark.parametrize("M", [1, 9, 16, 100, 129, 300])
+@pytest.mark.parametrize("dtype", [0, 1])
+@pytest.mark.parametrize("sym", [True, False])
+def test_prefill_small(cuda_lib, M, dtype, sym):
+    for i, (N, K) in enumerate(SMALL_SHAPES):
+        for G in (32, 64, 128):
+            if K % G:
+                continue
+            p = make_problem(M, N, K, G, sym, dtype, seed=2000 + 10 * i + G + M)
+            run_case(cuda_lib, p, PREFILL)
+
+
+@pytest.mark.parametrize("path", [DECODE, PREFILL])
+@pytest.mark.parametrize("dtype", [0, 1])
+@pytest.mark.parametrize("sym", [True, False])
+def test_integer_exact(cuda_lib, path, dtype, sym):
+    """s = 1, x integer in [-4, 4]: every fp32 partial sum is an exact
+    integer, so out must equal RN_dtype(y_ref) bit for bit."""
+    w = cuda_lib
+    M = 5 if path == DECODE else 200
+    for (N, K, G) in [(136, 288, 32), (392, 1088, 64), (264, 2560, 128)]:
+        p = make_problem(M, N, K, G, sym, dtype, seed=77 + N, x_kind="int4")
+        one = 0x3C00 if dtype == 0 else 0x3F80
+        p.scales[:] = one
+        d = to_device(p, w)
+        out = w.w4a16_gemm(d["x"], d["qweight"], d["scales"], d["qzeros"], G, path=path)
+        got = tensor_to_bits(out)
+        y_ref = oracle.gemm(p.x, M, K, d["ref_qw"], p.scales, d["ref_qz"], G, N, dtype)
+        assert np.all(y_ref == np.round(y_ref))
+        assert np.array_equal(got, oracle.round_array(y_ref, dtype)), (N, K, G)
+
+
+def test_tiny_symmetric_config(cuda_lib):
+    for M in (1, 4):
+        p = tiny_symmetric(M)
+        run_case(cuda_lib, p, 0)
+        run_case(cuda_lib, p, DECODE)
+        run_case(cuda_lib, p, PREFILL)
+
+
+def test_m_zero_is_noop(cuda_lib):
+    w = cuda_lib
+    p = make_problem(1, 64, 128, 32, True, 0, seed=3)
+    d = to_device(p, w)
+    out = torch.full((1, 64), 7.0, dtype=torch.float16, device="cuda")
+    x0 = d["x"][:0]
+    w.w4a16_gemm(x0, d["qweight"], d["scales"], None, 32, out=out[:0])
+    torch.cuda.synchronize()
+    assert torch.all(out == 7.0)
+
+
+def test_auto_dispatch_matches_forced(cuda_lib):
+    w = cuda_lib
+    for M in (1, 8, 9, 64):
+        p = make_problem(M, 264, 512, 64, False, 1, seed=500 + M)
+        d = to_device(p, w)
+        auto = tensor_to_bits(w.w4a16_gemm(d["x"], d["qweight"], d["scales"], d["qzeros"], 64))
+        path = w.w4a16_select_path(M, 264, 512, 64, False, 1)
+        forced = tensor_to_bits(w.w4a16_gemm(d["x"], d["qweight"], d["scales"], d["qzeros"], 64,
+                                             path=path))
+        assert np.array_equal(auto, forced)
+
+
+def test_deterministic(cuda_lib):
+    w = cuda_lib
+    for path, M in ((DECODE, 3), (PREFILL, 77)):
+        p = make_problem(M, 1032, 4096, 128, False, 1, seed=9)
+        d = to_device(p, w)
+        a = tensor_to_bits(w.w4a16_gemm(d["x"], d["qweight"], d["scales"], d["qzeros"], 128, path=path))
+        b = tensor_to_bits(w.w4a16_gemm(d["x"], d["qweight"], d["scales"], d["qzeros"], 128, path=path))
+        assert np.array_equal(a, b)
+
+
+def test_host_buffer_entry_point(cuda_lib):
+    w = cuda_lib
+    p = make_problem(3, 136, 288, 32, False, 0, seed=12)
+    d = to_device(p, w)
+    x_host = d["x"].cpu().pin_memory()
+    out_host = torch.empty((3, 136), dtype=torch.float16).pin_memory()
+    dev_x = torch.empty_like(d["x"])
+    dev_out = torch.empty((3, 136), dtype=torch.float16, device="cuda")
+    w.w4a16_gemm_host(x_host, d["qweight"], d["scales"], d["qzeros"], 32, out_host, dev_x, dev_out)
+    ref = w.w4a16_gemm(d["x"], d["qweight"], d["scales"], d["qzeros"], 32)
+    assert torch.equal(out_host, ref.cpu())
+
+
+def test_device_status_clean(cuda_lib):
+    torch.cuda.synchronize()
+    assert cuda_lib.w4a16_last_device_error() == 0

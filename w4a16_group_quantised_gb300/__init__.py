@@ -14,6 +14,7 @@ from .binding import (  # noqa: F401
     W4A16Error,
     library_path,
     load_library,
+    w4a16_debug_set_config,
     w4a16_dequant_debug,
     w4a16_gemm,
     w4a16_gemm_host,

@@ -56,11 +56,12 @@ def load_library():
             "w4a16_gemm_f16": [P, I, I, P, P, P, I, I, P, P],
             "w4a16_gemm_bf16": [P, I, I, P, P, P, I, I, P, P],
             "w4a16_gemm_ex": [P, I, I, P, P, P, I, I, P, P, I, I],
-            "w4a16_gemm_host": [P, I, I, P, P, P, I, I, P, I, P, P],
+            "w4a16_gemm_host": [P, I, I, P, P, P, I, I, P, I, P, P, P],
             "w4a16_select_path": [I, I, I, I, I, I],
             "w4a16_last_device_error": [],
             "w4a16_clear_device_error": [],
             "w4a16_version": [],
+            "w4a16_debug_set_config": [I, P, I],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -172,7 +173,7 @@ def w4a16_gemm_host(x_host, qweight, scales, qzeros, G: int, out_host, dev_x, de
     dt = _dtype_code(x_host)
     lib = load_library()
     rc = lib.w4a16_gemm_host(_p(x_host), M, K, _p(qweight), _p(scales), _p(qzeros), G, N,
-                             _p(out_host), dt, _p(dev_x), _p(dev_out))
+                             _p(out_host), dt, _p(dev_x), _p(dev_out), _stream_ptr(stream))
     _check("w4a16_gemm_host", rc)
     return out_host
 
@@ -180,6 +181,18 @@ def w4a16_gemm_host(x_host, qweight, scales, qzeros, G: int, out_host, dev_x, de
 def w4a16_select_path(M: int, N: int, K: int, G: int, sym: bool, dtype: int) -> int:
     """Which kernel the dispatcher picks: 1 = decode, 2 = prefill (host logic only)."""
     return load_library().w4a16_select_path(M, N, K, G, 1 if sym else 0, dtype)
+
+
+def w4a16_debug_set_config(which: int, vals=None) -> None:
+    """Tuning hook: which=1 decode {R, D, RW, KW, S}, which=2 prefill
+    {BN, stages, astages}, which=3 PDL {flag}; vals=None restores defaults."""
+    lib = load_library()
+    if vals is None:
+        rc = lib.w4a16_debug_set_config(which, None, 0)
+    else:
+        arr = (ctypes.c_int * len(vals))(*[int(v) for v in vals])
+        rc = lib.w4a16_debug_set_config(which, arr, len(vals))
+    _check("w4a16_debug_set_config", rc)
 
 
 def w4a16_last_device_error() -> int:

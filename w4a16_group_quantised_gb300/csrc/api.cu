@@ -1,0 +1,321 @@
+// api.cu -- the C ABI of include/w4a16.h: argument validation, per-device
+// state, the M dispatcher and the end-to-end host-buffer form.
+//
+// The dispatcher follows "[ROCm][Kernel] Add HybridW4A16LinearKernel: Triton
+// prefill + HIP skinny decode", PR description: small batch sizes (the page
+// uses M <= 5) go to the skinny split-K decode kernel, larger ones to the
+// fused-dequant GEMM.  Here the threshold is a measured table
+// (select_path_impl), bounded by the decode kernel's M <= 8.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <cstring>
+#include <functional>
+#include <mutex>
+
+#include "../../include/w4a16.h"
+#include "kernels.h"
+
+// Device status word: kernels whose bounded waits run out write here.
+__device__ int g_w4a16_status;
+
+namespace w4a16 {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DevState {
+    std::once_flag once;
+    int rc = W4A16_ERR_DEVICE;
+    DeviceInfo info{};
+};
+DevState g_dev[kMaxDevices];
+
+// Tuning overrides (process-wide), set through w4a16_debug_set_config.
+std::mutex g_cfg_mu;
+bool g_decode_override = false;
+DecodeCfg g_decode_cfg{};
+bool g_prefill_override = false;
+PrefillCfg g_prefill_cfg{};
+int g_pdl = 1;
+
+void init_device(DevState &st, int dev) {
+    DeviceInfo &d = st.info;
+    d.device = dev;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        st.rc = W4A16_ERR_CUDA;
+        return;
+    }
+    if (major != 10 || minor != 3) {  // the kernels are built for sm_103a only
+        st.rc = W4A16_ERR_DEVICE;
+        return;
+    }
+    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess) {
+        st.rc = W4A16_ERR_CUDA;
+        return;
+    }
+    void *sym = nullptr;
+    if (cudaGetSymbolAddress(&sym, g_w4a16_status) != cudaSuccess) {
+        st.rc = W4A16_ERR_CUDA;
+        return;
+    }
+    d.status = static_cast<int *>(sym);
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+        st.rc = W4A16_ERR_CUDA;
+        return;
+    }
+    d.encode_tiled = fn;
+    if (prefill_prepare_device(d) != cudaSuccess) {
+        st.rc = W4A16_ERR_CUDA;
+        return;
+    }
+    const char *e = std::getenv("W4A16_PDL");
+    if (e && e[0] == '0') g_pdl = 0;
+    st.rc = W4A16_OK;
+}
+
+int get_device(const DeviceInfo **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return W4A16_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return W4A16_ERR_DEVICE;
+    DevState &st = g_dev[dev];
+    std::call_once(st.once, init_device, std::ref(st), dev);
+    if (st.rc != W4A16_OK) return st.rc;
+    *out = &st.info;
+    return W4A16_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int validate_common(int M, int N, int K, int G, int dtype) {
+    if (dtype != W4A16_F16 && dtype != W4A16_BF16) return W4A16_ERR_DTYPE;
+    if (G != 32 && G != 64 && G != 128) return W4A16_ERR_GROUP;
+    if (M < 0 || N <= 0 || K <= 0) return W4A16_ERR_SHAPE;
+    if (K % G != 0) return W4A16_ERR_GROUP;
+    if (N % 8 != 0) return W4A16_ERR_SHAPE;
+    // int32 index headroom for the kernels' per-row arithmetic
+    if ((long long)N * (K / 8) >= (1LL << 31) || (long long)M * K >= (1LL << 31) ||
+        (long long)M * N >= (1LL << 31))
+        return W4A16_ERR_SHAPE;
+    return W4A16_OK;
+}
+
+int validate_gemm(const void *x, int M, int K, const int32_t *qw, const void *scales,
+                  const int32_t *qz, int G, int N, const void *out, int dtype) {
+    int rc = validate_common(M, N, K, G, dtype);
+    if (rc != W4A16_OK) return rc;
+    if (qw == nullptr || scales == nullptr) return W4A16_ERR_NULL;
+    if (M > 0 && (x == nullptr || out == nullptr)) return W4A16_ERR_NULL;
+    if (!aligned16(qw) || !aligned16(scales) || !aligned16(qz) || !aligned16(x) || !aligned16(out))
+        return W4A16_ERR_ALIGN;
+    return W4A16_OK;
+}
+
+// Largest M the decode kernel takes for this problem; measured crossover
+// between the two kernels (see the crossover sweep in the benchmark notes).
+int decode_max_m(int N, int K, int G, int sym, int dtype) {
+    (void)N; (void)K; (void)G; (void)sym; (void)dtype;
+    return W4A16_MAX_DECODE_M;
+}
+
+int select_path_impl(int M, int N, int K, int G, int sym, int dtype) {
+    return M <= decode_max_m(N, K, G, sym, dtype) ? W4A16_PATH_DECODE : W4A16_PATH_PREFILL;
+}
+
+int run_gemm(const void *x, int M, int K, const int32_t *qw, const void *scales, const int32_t *qz,
+             int G, int N, void *out, w4a16_stream_t stream, int dtype, int path) {
+    int rc = validate_gemm(x, M, K, qw, scales, qz, G, N, out, dtype);
+    if (rc != W4A16_OK) return rc;
+    if (path != W4A16_PATH_AUTO && path != W4A16_PATH_DECODE && path != W4A16_PATH_PREFILL)
+        return W4A16_ERR_ARG;
+    if (path == W4A16_PATH_DECODE && M > W4A16_MAX_DECODE_M) return W4A16_ERR_SHAPE;
+    if (M == 0) return W4A16_OK;
+    const DeviceInfo *dev = nullptr;
+    rc = get_device(&dev);
+    if (rc != W4A16_OK) return rc;
+    if (path == W4A16_PATH_AUTO) path = select_path_impl(M, N, K, G, qz == nullptr, dtype);
+
+    GemmArgs a{x, qw, scales, qz, out, M, N, K, G, dtype};
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (path == W4A16_PATH_DECODE) {
+        DecodeCfg c;
+        {
+            std::lock_guard<std::mutex> lk(g_cfg_mu);
+            c = g_decode_override ? g_decode_cfg
+                                  : decode_pick_cfg(M, N, K, G, qz == nullptr, dtype, dev->sm_count);
+        }
+        if (!decode_cfg_valid(c, M, K)) return W4A16_ERR_ARG;
+        e = launch_decode(a, c, *dev, s, g_pdl != 0);
+    } else {
+        PrefillCfg c;
+        {
+            std::lock_guard<std::mutex> lk(g_cfg_mu);
+            c = g_prefill_override ? g_prefill_cfg
+                                   : prefill_pick_cfg(M, N, K, G, qz == nullptr, dtype, dev->sm_count);
+        }
+        e = launch_prefill(a, c, *dev, s, g_pdl != 0);
+    }
+    return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace w4a16
+
+using namespace w4a16;
+
+extern "C" {
+
+int w4a16_pack(const uint8_t *q, int N, int K, int32_t *qweight, w4a16_stream_t stream) {
+    if (N < 0 || K < 0 || K % 8 != 0) return W4A16_ERR_SHAPE;
+    if ((long long)N * K >= (1LL << 34)) return W4A16_ERR_SHAPE;
+    if (N == 0 || K == 0) return W4A16_OK;
+    if (q == nullptr || qweight == nullptr) return W4A16_ERR_NULL;
+    if (!aligned16(q) || !aligned16(qweight)) return W4A16_ERR_ALIGN;
+    const DeviceInfo *dev = nullptr;
+    int rc = get_device(&dev);
+    if (rc != W4A16_OK) return rc;
+    return launch_pack(q, N, K, qweight, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? W4A16_OK
+               : W4A16_ERR_CUDA;
+}
+
+int w4a16_pack_zeros(const uint8_t *z, int N, int n_groups, int32_t *qzeros, w4a16_stream_t stream) {
+    if (N < 0 || n_groups < 0 || N % 8 != 0) return W4A16_ERR_SHAPE;
+    if ((long long)N * n_groups >= (1LL << 31)) return W4A16_ERR_SHAPE;
+    if (N == 0 || n_groups == 0) return W4A16_OK;
+    if (z == nullptr || qzeros == nullptr) return W4A16_ERR_NULL;
+    if (!aligned16(z) || !aligned16(qzeros)) return W4A16_ERR_ALIGN;
+    const DeviceInfo *dev = nullptr;
+    int rc = get_device(&dev);
+    if (rc != W4A16_OK) return rc;
+    return launch_pack_zeros(z, N, n_groups, qzeros, reinterpret_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? W4A16_OK
+               : W4A16_ERR_CUDA;
+}
+
+int w4a16_dequant_debug(const int32_t *qweight, const void *scales, const int32_t *qzeros_or_null,
+                        int G, int N, int K, void *out, w4a16_dtype_t dtype, w4a16_stream_t stream) {
+    int rc = validate_common(0, N, K, G, (int)dtype);
+    if (rc != W4A16_OK) return rc;
+    if (qweight == nullptr || scales == nullptr || out == nullptr) return W4A16_ERR_NULL;
+    if (!aligned16(qweight) || !aligned16(scales) || !aligned16(qzeros_or_null) || !aligned16(out))
+        return W4A16_ERR_ALIGN;
+    const DeviceInfo *dev = nullptr;
+    rc = get_device(&dev);
+    if (rc != W4A16_OK) return rc;
+    return launch_dequant(qweight, scales, qzeros_or_null, G, N, K, out, (int)dtype,
+                          reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? W4A16_OK
+               : W4A16_ERR_CUDA;
+}
+
+int w4a16_gemm(const void *x, int M, int K, const int32_t *qweight, const void *scales,
+               const int32_t *qzeros_or_null, int G, int N, void *out, w4a16_stream_t stream,
+               w4a16_dtype_t dtype) {
+    return run_gemm(x, M, K, qweight, scales, qzeros_or_null, G, N, out, stream, (int)dtype,
+                    W4A16_PATH_AUTO);
+}
+
+int w4a16_gemm_f16(const void *x, int M, int K, const int32_t *qweight, const void *scales,
+                   const int32_t *qzeros_or_null, int G, int N, void *out, w4a16_stream_t stream) {
+    return run_gemm(x, M, K, qweight, scales, qzeros_or_null, G, N, out, stream, W4A16_F16,
+                    W4A16_PATH_AUTO);
+}
+
+int w4a16_gemm_bf16(const void *x, int M, int K, const int32_t *qweight, const void *scales,
+                    const int32_t *qzeros_or_null, int G, int N, void *out, w4a16_stream_t stream) {
+    return run_gemm(x, M, K, qweight, scales, qzeros_or_null, G, N, out, stream, W4A16_BF16,
+                    W4A16_PATH_AUTO);
+}
+
+int w4a16_gemm_ex(const void *x, int M, int K, const int32_t *qweight, const void *scales,
+                  const int32_t *qzeros_or_null, int G, int N, void *out, w4a16_stream_t stream,
+                  w4a16_dtype_t dtype, w4a16_path_t path) {
+    return run_gemm(x, M, K, qweight, scales, qzeros_or_null, G, N, out, stream, (int)dtype, (int)path);
+}
+
+int w4a16_gemm_host(const void *x_host, int M, int K, const int32_t *qweight, const void *scales,
+                    const int32_t *qzeros_or_null, int G, int N, void *out_host, w4a16_dtype_t dtype,
+                    void *x_dev, void *out_dev, w4a16_stream_t stream) {
+    int rc = validate_gemm(x_dev, M, K, qweight, scales, qzeros_or_null, G, N, out_dev, (int)dtype);
+    if (rc != W4A16_OK) return rc;
+    if (M > 0 && (x_host == nullptr || out_host == nullptr)) return W4A16_ERR_NULL;
+    if (M == 0) return W4A16_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(x_dev, x_host, (size_t)M * K * 2, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return W4A16_ERR_CUDA;
+    rc = run_gemm(x_dev, M, K, qweight, scales, qzeros_or_null, G, N, out_dev, stream, (int)dtype,
+                  W4A16_PATH_AUTO);
+    if (rc != W4A16_OK) return rc;
+    if (cudaMemcpyAsync(out_host, out_dev, (size_t)M * N * 2, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return W4A16_ERR_CUDA;
+    return cudaStreamSynchronize(s) == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
+}
+
+int w4a16_select_path(int M, int N, int K, int G, int sym, int dtype) {
+    int rc = validate_common(M, N, K, G, dtype);
+    if (rc != W4A16_OK) return rc;
+    return select_path_impl(M, N, K, G, sym != 0, dtype);
+}
+
+int w4a16_last_device_error(void) {
+    const DeviceInfo *dev = nullptr;
+    int rc = get_device(&dev);
+    if (rc != W4A16_OK) return rc;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_w4a16_status, sizeof(int)) != cudaSuccess) return W4A16_ERR_CUDA;
+    return v;
+}
+
+int w4a16_clear_device_error(void) {
+    const DeviceInfo *dev = nullptr;
+    int rc = get_device(&dev);
+    if (rc != W4A16_OK) return rc;
+    int z = 0;
+    return cudaMemcpyToSymbol(g_w4a16_status, &z, sizeof(int)) == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
+}
+
+int w4a16_version(void) { return 100; }
+
+// Tuning hook: which = 1 sets the decode configuration {R, D, RW, KW, S},
+// which = 2 the prefill configuration {BN, stages, astages}; n = 0 clears it.
+// which = 3 sets programmatic dependent launch on (vals[0] != 0) or off.
+int w4a16_debug_set_config(int which, const int *vals, int n) {
+    std::lock_guard<std::mutex> lk(g_cfg_mu);
+    if (which == 1) {
+        if (n == 0) { g_decode_override = false; return W4A16_OK; }
+        if (n != 5 || vals == nullptr) return W4A16_ERR_ARG;
+        g_decode_cfg = DecodeCfg{vals[0], vals[1], vals[2], vals[3], vals[4]};
+        g_decode_override = true;
+        return W4A16_OK;
+    }
+    if (which == 2) {
+        if (n == 0) { g_prefill_override = false; return W4A16_OK; }
+        if (n != 3 || vals == nullptr) return W4A16_ERR_ARG;
+        if (vals[0] < 16 || vals[0] > 256 || vals[0] % 16 != 0 || vals[1] < 2 || vals[1] > 8 ||
+            vals[2] < 2 || vals[2] > 4)
+            return W4A16_ERR_ARG;
+        g_prefill_cfg = PrefillCfg{vals[0], vals[1], vals[2]};
+        g_prefill_override = true;
+        return W4A16_OK;
+    }
+    if (which == 3) {
+        if (n != 1 || vals == nullptr) return W4A16_ERR_ARG;
+        g_pdl = vals[0] != 0;
+        return W4A16_OK;
+    }
+    return W4A16_ERR_ARG;
+}
+
+}  // extern "C"

@@ -1,0 +1,59 @@
+// kernels.h -- internal interface between the C ABI (api.cu) and the kernel
+// translation units.  Not installed; the public interface is include/w4a16.h.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace w4a16 {
+
+struct GemmArgs {
+    const void *x;
+    const int32_t *qweight;
+    const void *scales;
+    const int32_t *qzeros;  // nullptr: symmetric
+    void *out;
+    int M, N, K, G;
+    int dtype;              // 0 fp16, 1 bf16
+};
+
+// Per-device facts the launchers need.
+struct DeviceInfo {
+    int device;
+    int sm_count;
+    int max_smem_optin;
+    int *status;            // device address of the status word
+    void *encode_tiled;     // cuTensorMapEncodeTiled entry point
+};
+
+// ---- pack.cu
+cudaError_t launch_pack(const uint8_t *q, int N, int K, int32_t *qweight, cudaStream_t s);
+cudaError_t launch_pack_zeros(const uint8_t *z, int N, int ng, int32_t *qzeros, cudaStream_t s);
+cudaError_t launch_dequant(const int32_t *qweight, const void *scales, const int32_t *qzeros,
+                           int G, int N, int K, void *out, int dtype, cudaStream_t s);
+
+// ---- decode.cu
+struct DecodeCfg {
+    int R;    // 16-row blocks per warp
+    int D;    // pipeline depth (register ring of weight steps)
+    int RW;   // warps along rows in a CTA
+    int KW;   // warps along K in a CTA
+    int S;    // CTAs along K in a cluster (1..8)
+};
+DecodeCfg decode_pick_cfg(int M, int N, int K, int G, int sym, int dtype, int sm_count);
+bool decode_cfg_valid(const DecodeCfg &c, int M, int K);
+size_t decode_smem_bytes(const DecodeCfg &c, int M, int K);
+cudaError_t launch_decode(const GemmArgs &a, const DecodeCfg &c, const DeviceInfo &dev,
+                          cudaStream_t s, bool pdl);
+
+// ---- prefill.cu
+struct PrefillCfg {
+    int BN;       // tokens per tile (MMA N), multiple of 16, <= 256
+    int stages;   // TMA stages (x + raw weights)
+    int astages;  // dequantised-weight stages
+};
+PrefillCfg prefill_pick_cfg(int M, int N, int K, int G, int sym, int dtype, int sm_count);
+cudaError_t launch_prefill(const GemmArgs &a, const PrefillCfg &c, const DeviceInfo &dev,
+                           cudaStream_t s, bool pdl);
+cudaError_t prefill_prepare_device(const DeviceInfo &dev);
+
+}  // namespace w4a16
