@@ -147,9 +147,12 @@ int w4a16_clear_device_error(void);
 int w4a16_version(void);
 
 /* Tuning hook (process-wide, for benchmarks and sweeps).  which = 1: decode
- * configuration vals = {R, D, RW, KW, S} (16-row blocks per warp, register
- * pipeline depth, row warps, K warps, cluster CTAs along K), n = 5;
- * which = 2: prefill configuration vals = {BN, stages, astages}, n = 3;
+ * configuration vals = {R, NW, NB, NS, S} (16-row blocks per warp, warps per
+ * CTA, 128-wide TMA boxes per ring stage, ring stages, cluster CTAs along
+ * K), n = 5;
+ * which = 2: prefill configuration vals = {BN, x-ring stages, dequantised-
+ * weight stages, packed-weight stages}, n = 4 (BN a multiple of 16 in
+ * [16, 256]; the rings must fit in shared memory);
  * which = 3: programmatic dependent launch on/off, vals = {flag}, n = 1.
  * n = 0 restores the built-in choice for which = 1 or 2.  An invalid
  * configuration is rejected here or, for the decode shape limits, by the

@@ -108,10 +108,12 @@ def test_dispatcher_is_host_logic(lib):
 
 
 def test_debug_config_validation(lib):
-    arr = (ctypes.c_int * 3)(24, 4, 3)
-    assert lib.w4a16_debug_set_config(2, arr, 3) == -9   # BN not a multiple of 16
-    arr = (ctypes.c_int * 3)(128, 4, 3)
-    assert lib.w4a16_debug_set_config(2, arr, 3) == 0
+    arr = (ctypes.c_int * 4)(24, 3, 2, 2)
+    assert lib.w4a16_debug_set_config(2, arr, 4) == -9   # BN not a multiple of 16
+    arr = (ctypes.c_int * 4)(256, 8, 2, 2)
+    assert lib.w4a16_debug_set_config(2, arr, 4) == -9   # rings do not fit in shared memory
+    arr = (ctypes.c_int * 4)(128, 3, 2, 2)
+    assert lib.w4a16_debug_set_config(2, arr, 4) == 0
     assert lib.w4a16_debug_set_config(2, None, 0) == 0
     assert lib.w4a16_debug_set_config(9, None, 0) == -9
 

@@ -14,7 +14,7 @@
 #include <functional>
 #include <mutex>
 
-#include "../../include/w4a16.h"
+#include "w4a16.h"
 #include "kernels.h"
 
 // Device status word: kernels whose bounded waits run out write here.
@@ -154,7 +154,7 @@ int run_gemm(const void *x, int M, int K, const int32_t *qw, const void *scales,
             c = g_decode_override ? g_decode_cfg
                                   : decode_pick_cfg(M, N, K, G, qz == nullptr, dtype, dev->sm_count);
         }
-        if (!decode_cfg_valid(c, M, K)) return W4A16_ERR_ARG;
+        if (!decode_cfg_valid(c, M, K, G, qz != nullptr)) return W4A16_ERR_ARG;
         e = launch_decode(a, c, *dev, s, g_pdl != 0);
     } else {
         PrefillCfg c;
@@ -288,8 +288,9 @@ int w4a16_clear_device_error(void) {
 
 int w4a16_version(void) { return 100; }
 
-// Tuning hook: which = 1 sets the decode configuration {R, D, RW, KW, S},
-// which = 2 the prefill configuration {BN, stages, astages}; n = 0 clears it.
+// Tuning hook: which = 1 sets the decode configuration {R, NW, NB, NS, S},
+// which = 2 the prefill configuration {BN, x stages, A stages, W stages};
+// n = 0 clears it.
 // which = 3 sets programmatic dependent launch on (vals[0] != 0) or off.
 int w4a16_debug_set_config(int which, const int *vals, int n) {
     std::lock_guard<std::mutex> lk(g_cfg_mu);
@@ -302,11 +303,10 @@ int w4a16_debug_set_config(int which, const int *vals, int n) {
     }
     if (which == 2) {
         if (n == 0) { g_prefill_override = false; return W4A16_OK; }
-        if (n != 3 || vals == nullptr) return W4A16_ERR_ARG;
-        if (vals[0] < 16 || vals[0] > 256 || vals[0] % 16 != 0 || vals[1] < 2 || vals[1] > 8 ||
-            vals[2] < 2 || vals[2] > 4)
-            return W4A16_ERR_ARG;
-        g_prefill_cfg = PrefillCfg{vals[0], vals[1], vals[2]};
+        if (n != 4 || vals == nullptr) return W4A16_ERR_ARG;
+        PrefillCfg c{vals[0], vals[1], vals[2], vals[3]};
+        if (!prefill_cfg_valid(c)) return W4A16_ERR_ARG;
+        g_prefill_cfg = c;
         g_prefill_override = true;
         return W4A16_OK;
     }

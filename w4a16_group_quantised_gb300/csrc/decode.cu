@@ -8,24 +8,31 @@
 // section "Upstream's Python side is kept -- and it does NOT work here").
 //
 // Design (GB300-first, not the pages' RDNA kernel):
-//  * A warp owns R blocks of 16 weight rows and a slice of K.  Each lane
-//    streams 16 bytes (32 weights) of rows g and g+8 per 128-wide K step with
-//    non-allocating 128-bit loads, D steps deep in a register ring.
-//  * Weights are dequantised in registers (dq_word_i4) and multiplied on the
-//    tensor cores with mma.sync m16n8k16 (fp32 accumulate): A = 16 weight rows
-//    x 16 k, B = x^T (k x 8 batch columns, rows >= M are zero).  The k order
-//    inside an MMA is a permutation of the word's nibbles; the x operand is
-//    staged in shared memory in the same permutation, so the dot product is
-//    the plain one.
-//  * Split-K: KW warps of a CTA and S CTAs of a thread-block cluster take
-//    disjoint K slices; partial sums meet in shared memory and are reduced
-//    across the cluster through distributed shared memory, in a fixed order
-//    (deterministic, no global workspace, no atomics).
-//  * Programmatic dependent launch: the first weight steps are loaded before
-//    the grid-dependency wait; x and out are touched only after it.
-//    Weights, scales and zero points must therefore not be written by the
-//    immediately preceding kernel if that kernel triggers early launch.
+//  * A CTA owns RT = 16 * R * NW weight rows and one K slice.  One thread
+//    streams the slice's packed weights through an NS-stage shared-memory
+//    ring with 2-D TMA boxes of RT rows x 128 k (64 bytes a row, so a warp's
+//    16-byte reads of rows g and g+1 fall on disjoint banks); up to
+//    NS * NB boxes are in flight per CTA from the first cycle.  Scales and
+//    zero points of the slice are staged once; x is staged permuted.
+//  * Each warp owns R blocks of 16 rows.  Per 128-wide K step a lane takes
+//    4 words (32 weights) of rows g and g+8, dequantises them in registers
+//    (dq_word_i4) and multiplies on the tensor cores with mma.sync m16n8k16
+//    (fp32 accumulate): A = 16 weight rows x 16 k, B = x^T (k x 8 batch
+//    columns, rows >= M are zero).  The k order inside an MMA is a
+//    permutation of each word's nibbles; x is staged in the same
+//    permutation, so the dot product is the plain one.
+//  * Split-K across the S CTAs of a thread-block cluster: partial sums meet
+//    in shared memory and are reduced through distributed shared memory in
+//    a fixed order (deterministic, no global workspace, no atomics).
+//  * Programmatic dependent launch: weights, scales and zero points are
+//    requested before the grid-dependency wait; x and out are touched only
+//    after it.  Weights, scales and zero points must therefore not be
+//    written by the immediately preceding kernel if that kernel triggers
+//    early launch.
+//  * Every mbarrier wait is bounded; on a timeout the status word is set and
+//    the CTA leaves its loop.
 #include <cooperative_groups.h>
+#include <cuda.h>
 
 #include "dequant.cuh"
 #include "kernels.h"
@@ -35,17 +42,20 @@ namespace cg = cooperative_groups;
 
 namespace w4a16 {
 
+constexpr int kBoxK = 128;             // k per TMA box (16 int32 words = 64 B a row)
+constexpr int kBoxRowBytes = kBoxK / 2;
+
 struct DecodeParams {
     const uint16_t *x;
-    const int32_t *qw;
     const uint16_t *scales;
     const int32_t *qz;
     uint16_t *out;
-    int M, N, K, G, ng;
-    int RW, KW, S;
-    int nblk;    // full 128-wide K blocks
-    int ntail;   // trailing 32-wide K units (0..3)
-    int xpitch;  // bytes per x row in shared memory
+    int *status;
+    int M, N, K, G, ng, log2G;
+    int NW, NB, NS, S;
+    int nblk;        // K blocks of 128 (the last one may be partial)
+    int xpitch;      // bytes per x row in shared memory
+    int gmax;        // max groups per CTA slice
 };
 
 template <int DT>
@@ -65,13 +75,6 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
             : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
     }
 }
-
-template <int R>
-struct WStep {
-    uint4 wa[R], wb[R];      // 4 words of rows g and g+8, per row block
-    uint32_t sa[R], sb[R];   // scale bits
-    uint32_t za[R], zb[R];   // zero-point words (asymmetric)
-};
 
 template <int DT>
 __device__ __forceinline__ uint16_t f32_to_dt(float v) {
@@ -96,87 +99,117 @@ __device__ __forceinline__ void mac_word(float (&acc)[4], uint32_t wa, uint32_t 
     mma_16816<DT>(acc, oa[2], ob[2], oa[3], ob[3], xv.z, xv.w);
 }
 
-template <int DT, bool ASYM, int R, int D>
-__global__ void __launch_bounds__(256) decode_kernel(const DecodeParams p) {
-    extern __shared__ __align__(128) unsigned char smem[];
+struct DecodeSmem {
+    uint32_t ring, scales, zeros, x, red, bars, total;
+};
+
+__host__ __device__ inline DecodeSmem decode_layout(int R, int NW, int NB, int NS, int M, int xpitch,
+                                                    int gmax, bool asym) {
+    const int RT = 16 * R * NW;
+    DecodeSmem L;
+    uint32_t off = 0;
+    L.ring = off;                                   // 128-B aligned for TMA
+    off += (uint32_t)NS * NB * RT * kBoxRowBytes;
+    L.scales = off;                                 // [RT][gmax] uint16
+    off += (uint32_t)RT * gmax * 2;
+    off = (off + 15u) & ~15u;
+    L.zeros = off;                                  // [RT/8][gmax] uint32
+    off += asym ? (uint32_t)(RT / 8) * gmax * 4 : 0u;
+    off = (off + 127u) & ~127u;
+    L.x = off;                                      // [M][xpitch]
+    off += (uint32_t)M * xpitch;
+    L.red = off;                                    // [NW*R][16][8] fp32
+    off += (uint32_t)NW * R * 16 * 8 * 4;
+    L.bars = off;
+    off += (uint32_t)2 * NS * 8 + 16;
+    L.total = off + 128;                            // slack to align the base to 128
+    return L;
+}
+
+template <int DT, bool ASYM, int R>
+__global__ void __launch_bounds__(256) decode_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                                                     const DecodeParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~(uintptr_t)127);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
-    const int RW = p.RW, KW = p.KW, S = p.S;
-    const int rw = warp % RW, kw = warp / RW;
+    const int NW = p.NW, NB = p.NB, NS = p.NS, S = p.S;
+    const int RT = 16 * R * NW;
     const int rank = (S > 1) ? (int)cg::this_cluster().block_rank() : 0;
     const int tile = blockIdx.x / S;
-    const int rows_cta = 16 * R * RW;
-    const int K8 = p.K >> 3;
+    const int n_tile0 = tile * RT;
+    const DecodeSmem L = decode_layout(R, NW, NB, NS, p.M, p.xpitch, p.gmax, ASYM);
 
     grid_dependents_launch();
 
-    // ---- K slices: CTA (cluster rank) and warp (kw) ranges of 128-wide blocks
-    const int NS = S * KW;
-    const int cta_b0 = (int)((long long)rank * p.nblk / S);
-    const int cta_b1 = (int)((long long)(rank + 1) * p.nblk / S);
-    const int slice = rank * KW + kw;
-    const int sb = (int)((long long)slice * p.nblk / NS);
-    const int se = (int)((long long)(slice + 1) * p.nblk / NS);
-    const bool last_cta = (rank == S - 1);
-    const bool tail_warp = (slice == NS - 1) && p.ntail > 0;
-    const int nsteps = se - sb;
+    // ---- K slice of this CTA, in 128-wide blocks
+    const int b0 = (int)((long long)rank * p.nblk / S);
+    const int b1 = (int)((long long)(rank + 1) * p.nblk / S);
+    const int nb = b1 - b0;
+    const int nsteps = (nb + NB - 1) / NB;          // ring stages to consume
+    const int g0 = (b0 * kBoxK) / p.G;              // first group of the slice
+    const int g1 = min(p.ng, (b1 * kBoxK + p.G - 1) / p.G);
+    const int ngs = g1 - g0;
 
-    // ---- rows of this warp
-    int rowA[R];
-    bool vA[R], vB[R];
-#pragma unroll
-    for (int rb = 0; rb < R; ++rb) {
-        int n0 = tile * rows_cta + (rw * R + rb) * 16;
-        rowA[rb] = n0 + g;
-        vA[rb] = rowA[rb] < p.N;
-        vB[rb] = rowA[rb] + 8 < p.N;
-    }
+    const uint32_t ring = smem_u32(smem + L.ring);
+    const uint32_t stage_bytes = (uint32_t)NB * RT * kBoxRowBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
+    const uint32_t bar0 = smem_u32(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (NS + s); };
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.bars + 16 * NS);
 
-    auto load_step = [&](WStep<R> &st, int blk) {
-        const int grp = (blk * 128 + 32 * t) / p.G;
-#pragma unroll
-        for (int rb = 0; rb < R; ++rb) {
-            const int ra = rowA[rb], rbw = ra + 8;
-            const int32_t *wa = p.qw + (size_t)ra * K8 + blk * 16 + 4 * t;
-            const int32_t *wb = p.qw + (size_t)rbw * K8 + blk * 16 + 4 * t;
-            st.wa[rb] = vA[rb] ? ldg_stream_v4(wa) : make_uint4(0, 0, 0, 0);
-            st.wb[rb] = vB[rb] ? ldg_stream_v4(wb) : make_uint4(0, 0, 0, 0);
-            st.sa[rb] = vA[rb] ? (uint32_t)__ldg(p.scales + (size_t)ra * p.ng + grp) : 0u;
-            st.sb[rb] = vB[rb] ? (uint32_t)__ldg(p.scales + (size_t)rbw * p.ng + grp) : 0u;
-            if (ASYM) {
-                const int zr = (ra - g) >> 3;  // first row of the block is a multiple of 16
-                st.za[rb] = vA[rb] ? (uint32_t)__ldg(p.qz + (size_t)zr * p.ng + grp) : 0u;
-                st.zb[rb] = vB[rb] ? (uint32_t)__ldg(p.qz + (size_t)(zr + 1) * p.ng + grp) : 0u;
-            }
-        }
+    auto issue = [&](int step) {  // one thread: TMA all boxes of a ring stage
+        const int s = step % NS;
+        const int bb = b0 + step * NB;
+        const int nbox = min(NB, b1 - bb);
+        mbar_arrive_expect_tx(full_bar(s), (uint32_t)nbox * RT * kBoxRowBytes);
+        for (int j = 0; j < nbox; ++j)
+            tma_load_2d(ring + (uint32_t)s * stage_bytes + (uint32_t)j * RT * kBoxRowBytes, &tmap_w,
+                        full_bar(s), (bb + j) * (kBoxK / 8), n_tile0);
     };
 
-    WStep<R> ring[D];
-#pragma unroll
-    for (int d = 0; d < D - 1; ++d)
-        if (d < nsteps) load_step(ring[d], sb + d);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), NW);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmap_w);
+        for (int st = 0; st < min(NS, nsteps); ++st) issue(st);
+    }
 
-    // ---- x slice of this CTA -> shared memory (permuted), after the
-    //      grid-dependency wait (x may be produced by the previous kernel).
-    float *red = reinterpret_cast<float *>(smem);
-    const int red_floats = KW * RW * R * 16 * 8;
-    unsigned char *xs = smem + red_floats * 4;
+    // ---- scales and zero points of the slice (static: before the dependency wait)
+    uint16_t *s_sc = reinterpret_cast<uint16_t *>(smem + L.scales);
+    for (int i = threadIdx.x; i < RT * ngs; i += blockDim.x) {
+        const int r = i / ngs, gg = i % ngs;
+        const int n = n_tile0 + r;
+        s_sc[r * p.gmax + gg] = n < p.N ? __ldg(p.scales + (size_t)n * p.ng + g0 + gg) : (uint16_t)0;
+    }
+    if (ASYM) {
+        uint32_t *s_z = reinterpret_cast<uint32_t *>(smem + L.zeros);
+        for (int i = threadIdx.x; i < (RT / 8) * ngs; i += blockDim.x) {
+            const int r8 = i / ngs, gg = i % ngs;
+            const int n8 = n_tile0 / 8 + r8;
+            s_z[r8 * p.gmax + gg] = n8 < p.N / 8 ? (uint32_t)__ldg(p.qz + (size_t)n8 * p.ng + g0 + gg) : 0u;
+        }
+    }
+
+    // ---- x slice -> shared memory, permuted; zero beyond K and for k >= K
     grid_dependency_wait();
+    unsigned char *xs = smem + L.x;
     {
-        const int cnb = cta_b1 - cta_b0;
-        const int nch = cnb * 16 + (last_cta ? p.ntail * 4 : 0);
-        const int kbase = cta_b0 * 128;
-        const int total = p.M * nch;
-        for (int i = threadIdx.x; i < total; i += blockDim.x) {
+        const int nch = nb * 16;                   // 16-byte chunks per row
+        const int kbase = b0 * kBoxK;
+        for (int i = threadIdx.x; i < p.M * nch; i += blockDim.x) {
             const int m = i / nch, c = i % nch;
-            uint4 v = *reinterpret_cast<const uint4 *>(p.x + (size_t)m * p.K + kbase + 8 * c);
-            int pos;
-            if (c < cnb * 16) {
-                const int b = c >> 4, cc = c & 15;
-                pos = b * 16 + (cc & 3) * 4 + (cc >> 2);  // chunk 4t+w stored at 4w+t
-            } else {
-                pos = c;
-            }
+            const int k = kbase + 8 * c;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (k < p.K) v = *reinterpret_cast<const uint4 *>(p.x + (size_t)m * p.K + k);
+            const int b = c >> 4, cc = c & 15;
+            const int pos = b * 16 + (cc & 3) * 4 + (cc >> 2);   // chunk 4t+w stored at 4w+t
             uint4 o;
             o.x = __byte_perm(v.x, v.z, 0x5410);  // (x0, x4)
             o.y = __byte_perm(v.x, v.z, 0x7632);  // (x1, x5)
@@ -187,168 +220,176 @@ __global__ void __launch_bounds__(256) decode_kernel(const DecodeParams p) {
     }
     __syncthreads();
 
-    float acc[R][4];
+    // Two independent accumulator chains per row block, so consecutive MMAs
+    // do not wait on each other's results.
+    float acc[R][4], acc2[R][4];
 #pragma unroll
-    for (int rb = 0; rb < R; ++rb) acc[rb][0] = acc[rb][1] = acc[rb][2] = acc[rb][3] = 0.f;
+    for (int rb = 0; rb < R; ++rb)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[rb][e] = acc2[rb][e] = 0.f;
 
     const bool has_x = g < p.M;
     const unsigned char *xrow = xs + (size_t)g * p.xpitch;
+    const uint16_t *s_sc_c = s_sc;
+    const uint32_t *s_z = reinterpret_cast<const uint32_t *>(smem + L.zeros);
+    const int rloc0 = warp * R * 16 + g;            // row of rb = 0 within the tile
 
-    auto compute_step = [&](const WStep<R> &st, int blk) {
-        const int lb = blk - cta_b0;
-        uint4 xv[4];
-#pragma unroll
-        for (int w = 0; w < 4; ++w)
-            xv[w] = has_x ? *reinterpret_cast<const uint4 *>(xrow + (lb * 16 + 4 * w + t) * 16)
-                          : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int rb = 0; rb < R; ++rb) {
-            uint32_t zA = 8u, zB = 8u;
-            if (ASYM) {
-                zA = (st.za[rb] >> (4 * g)) & 0xFu;
-                zB = (st.zb[rb] >> (4 * g)) & 0xFu;
-            }
-            const uint32_t zla = zlo2<DT>(zA), zha = zhi2<DT>(zA), s2a = rep2(st.sa[rb]);
-            const uint32_t zlb = zlo2<DT>(zB), zhb = zhi2<DT>(zB), s2b = rep2(st.sb[rb]);
-            mac_word<DT>(acc[rb], st.wa[rb].x, st.wb[rb].x, zla, zha, s2a, zlb, zhb, s2b, xv[0]);
-            mac_word<DT>(acc[rb], st.wa[rb].y, st.wb[rb].y, zla, zha, s2a, zlb, zhb, s2b, xv[1]);
-            mac_word<DT>(acc[rb], st.wa[rb].z, st.wb[rb].z, zla, zha, s2a, zlb, zhb, s2b, xv[2]);
-            mac_word<DT>(acc[rb], st.wa[rb].w, st.wb[rb].w, zla, zha, s2a, zlb, zhb, s2b, xv[3]);
+    bool ok = true;
+    for (int step = 0; step < nsteps && ok; ++step) {
+        const int s = step % NS;
+        // refill the slot used one step ago, once every warp has left it
+        if (threadIdx.x == 0 && step > 0 && step - 1 + NS < nsteps) {
+            const int ps = (step - 1) % NS;
+            if (mbar_wait_bounded(empty_bar(ps), (uint32_t)(((step - 1) / NS) & 1), p.status, abort_flag))
+                issue(step - 1 + NS);
         }
-    };
-
-    for (int s0 = 0; s0 < nsteps; s0 += D) {
-#pragma unroll
-        for (int d = 0; d < D; ++d) {
-            const int s = s0 + d;
-            if (s < nsteps) {
-                if (s + D - 1 < nsteps) load_step(ring[(d + D - 1) % D], sb + s + D - 1);
-                compute_step(ring[d], sb + s);
-            }
+        if (!mbar_wait_bounded(full_bar(s), (uint32_t)((step / NS) & 1), p.status, abort_flag)) {
+            ok = false;
+            break;
         }
-    }
-
-    // ---- trailing 32-wide units (K % 128), taken by the last slice
-    if (tail_warp) {
-        const int cnb = cta_b1 - cta_b0;
-        for (int u = 0; u < p.ntail; ++u) {
-            const int k0 = p.nblk * 128 + 32 * u;
-            const int grp = k0 / p.G;
-            uint4 xv = has_x ? *reinterpret_cast<const uint4 *>(xrow + (cnb * 16 + 4 * u + t) * 16)
-                             : make_uint4(0, 0, 0, 0);
+        const unsigned char *stage = smem + L.ring + (size_t)s * stage_bytes;
+        const int nbox = min(NB, b1 - (b0 + step * NB));
+        for (int j = 0; j < nbox; ++j) {
+            const int lb = step * NB + j;                 // local block index
+            const int kb = (b0 + lb) * kBoxK;             // first k of the block
+            const int gl = ((kb + 32 * t) >> p.log2G) - g0;  // this lane's group, slice-local
+            const bool kin = kb + 32 * t < p.K;
+            uint4 xv[4];
+#pragma unroll
+            for (int w = 0; w < 4; ++w)
+                xv[w] = has_x ? *reinterpret_cast<const uint4 *>(xrow + (lb * 16 + 4 * w + t) * 16)
+                              : make_uint4(0, 0, 0, 0);
+            const unsigned char *box = stage + (size_t)j * RT * kBoxRowBytes;
 #pragma unroll
             for (int rb = 0; rb < R; ++rb) {
-                const int ra = rowA[rb], rbw = ra + 8;
-                uint32_t wa = vA[rb] ? ldg_stream_u32(p.qw + (size_t)ra * K8 + k0 / 8 + t) : 0u;
-                uint32_t wb = vB[rb] ? ldg_stream_u32(p.qw + (size_t)rbw * K8 + k0 / 8 + t) : 0u;
-                uint32_t sa = vA[rb] ? (uint32_t)__ldg(p.scales + (size_t)ra * p.ng + grp) : 0u;
-                uint32_t sbv = vB[rb] ? (uint32_t)__ldg(p.scales + (size_t)rbw * p.ng + grp) : 0u;
-                uint32_t zA = 8u, zB = 8u;
-                if (ASYM) {
-                    const int zr = (ra - g) >> 3;
-                    zA = vA[rb] ? ((uint32_t)__ldg(p.qz + (size_t)zr * p.ng + grp) >> (4 * g)) & 0xFu : 0u;
-                    zB = vB[rb] ? ((uint32_t)__ldg(p.qz + (size_t)(zr + 1) * p.ng + grp) >> (4 * g)) & 0xFu
-                                : 0u;
+                const int ra = rloc0 + rb * 16, rbw = ra + 8;
+                const uint4 wa = *reinterpret_cast<const uint4 *>(box + ra * kBoxRowBytes + 16 * t);
+                const uint4 wb = *reinterpret_cast<const uint4 *>(box + rbw * kBoxRowBytes + 16 * t);
+                uint32_t sa = 0u, sb = 0u, zA = 8u, zB = 8u;
+                if (kin) {
+                    sa = s_sc_c[ra * p.gmax + gl];
+                    sb = s_sc_c[rbw * p.gmax + gl];
+                    if (ASYM) {
+                        zA = (s_z[(ra >> 3) * p.gmax + gl] >> (4 * g)) & 0xFu;
+                        zB = (s_z[(rbw >> 3) * p.gmax + gl] >> (4 * g)) & 0xFu;
+                    }
                 }
-                mac_word<DT>(acc[rb], wa, wb, zlo2<DT>(zA), zhi2<DT>(zA), rep2(sa), zlo2<DT>(zB),
-                             zhi2<DT>(zB), rep2(sbv), xv);
+                const uint32_t zla = zlo2<DT>(zA), zha = zhi2<DT>(zA), s2a = rep2(sa);
+                const uint32_t zlb = zlo2<DT>(zB), zhb = zhi2<DT>(zB), s2b = rep2(sb);
+                mac_word<DT>(acc[rb], wa.x, wb.x, zla, zha, s2a, zlb, zhb, s2b, xv[0]);
+                mac_word<DT>(acc2[rb], wa.y, wb.y, zla, zha, s2a, zlb, zhb, s2b, xv[1]);
+                mac_word<DT>(acc[rb], wa.z, wb.z, zla, zha, s2a, zlb, zhb, s2b, xv[2]);
+                mac_word<DT>(acc2[rb], wa.w, wb.w, zla, zha, s2a, zlb, zhb, s2b, xv[3]);
             }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(s));
     }
 
-    // ---- partial sums -> shared memory: red[kw][row block][16][8]
+    // ---- partial sums -> shared memory: red[row block][16][8]
+    float *red = reinterpret_cast<float *>(smem + L.red);
+#pragma unroll
+    for (int rb = 0; rb < R; ++rb)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[rb][e] += acc2[rb][e];
 #pragma unroll
     for (int rb = 0; rb < R; ++rb) {
-        float *r = red + ((size_t)(kw * RW * R + rw * R + rb) * 16) * 8;
+        float *r = red + ((size_t)(warp * R + rb) * 16) * 8;
         r[g * 8 + 2 * t] = acc[rb][0];
         r[g * 8 + 2 * t + 1] = acc[rb][1];
         r[(g + 8) * 8 + 2 * t] = acc[rb][2];
         r[(g + 8) * 8 + 2 * t + 1] = acc[rb][3];
     }
-
     if (S > 1) {
         cg::this_cluster().sync();
     } else {
         __syncthreads();
     }
 
-    // ---- reduce over KW warps and S cluster ranks; rank r writes its share
+    // ---- reduce over the S cluster ranks; rank r writes its share of outputs
     {
-        const int total = rows_cta * p.M;
+        const int total = RT * p.M;
         const int i0 = (int)((long long)rank * total / S);
         const int i1 = (int)((long long)(rank + 1) * total / S);
         for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
-            const int m = i / rows_cta, row = i % rows_cta;
-            const int n = tile * rows_cta + row;
+            const int m = i / RT, row = i % RT;
+            const int n = n_tile0 + row;
             if (n >= p.N) continue;
-            const int off = ((row >> 4) * 16 + (row & 15)) * 8 + m;
+            const int off = row * 8 + m;
             float sum = 0.f;
             for (int s = 0; s < S; ++s) {
                 const float *rs = (S > 1) ? cg::this_cluster().map_shared_rank(red, s) : red;
-                for (int k = 0; k < KW; ++k) sum += rs[(size_t)k * RW * R * 128 + off];
+                sum += rs[off];
             }
             p.out[(size_t)m * p.N + n] = f32_to_dt<DT>(sum);
         }
     }
-
     if (S > 1) cg::this_cluster().sync();  // keep shared memory alive for readers
 }
 
 // ------------------------------------------------------------------ host side
-static int xpitch_bytes(const DecodeCfg &c, int K) {
-    const int nblk = K / 128, ntail = (K % 128) / 32;
-    const int max_cnb = (nblk + c.S - 1) / c.S;
-    int bytes = max_cnb * 256 + ntail * 64;
-    bytes = ((bytes + 127) / 128) * 128 + 64;  // odd multiple of 64: rows g, g+1 on different banks
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static int decode_gmax(const DecodeCfg &c, int K, int G) {
+    const int nblk = (K + kBoxK - 1) / kBoxK;
+    const int max_nb = (nblk + c.S - 1) / c.S;
+    return (max_nb * kBoxK) / G + 2;
+}
+
+static int decode_xpitch(const DecodeCfg &c, int K) {
+    const int nblk = (K + kBoxK - 1) / kBoxK;
+    const int max_nb = (nblk + c.S - 1) / c.S;
+    int bytes = max_nb * 256;
+    bytes = ((bytes + 127) / 128) * 128 + 64;  // odd multiple of 64: rows g, g+1 on other banks
     return bytes;
 }
 
-size_t decode_smem_bytes(const DecodeCfg &c, int M, int K) {
-    const size_t red = (size_t)c.KW * c.RW * c.R * 16 * 8 * 4;
-    return red + (size_t)M * xpitch_bytes(c, K);
+size_t decode_smem_bytes(const DecodeCfg &c, int M, int K, int G, bool asym) {
+    return decode_layout(c.R, c.NW, c.NB, c.NS, M, decode_xpitch(c, K), decode_gmax(c, K, G), asym).total;
 }
 
-bool decode_cfg_valid(const DecodeCfg &c, int M, int K) {
+bool decode_cfg_valid(const DecodeCfg &c, int M, int K, int G, bool asym) {
     if (c.R != 1 && c.R != 2) return false;
-    if (c.D != 2 && c.D != 4) return false;
-    if (c.RW < 1 || c.KW < 1 || c.RW * c.KW > 8) return false;
+    if (c.NW != 1 && c.NW != 2 && c.NW != 4 && c.NW != 8) return false;
+    if (c.NB < 1 || c.NB > 8) return false;
+    if (c.NS < 2 || c.NS > 8) return false;
     if (c.S < 1 || c.S > 8) return false;
-    if (decode_smem_bytes(c, M, K) > 200 * 1024) return false;
+    if (16 * c.R * c.NW > 256) return false;        // TMA box height limit
+    if (decode_smem_bytes(c, M, K, G, asym) > 220 * 1024) return false;
     return true;
 }
 
 DecodeCfg decode_pick_cfg(int M, int N, int K, int G, int sym, int dtype, int sm_count) {
-    (void)G; (void)sym; (void)dtype;
-    DecodeCfg c{1, 4, 4, 1, 1};
-    const int nblk = K / 128;
-    const int row_blocks = (N + 15) / 16;
-    const int target_warps = sm_count * 16;
-    int ks = (target_warps + row_blocks - 1) / row_blocks;
-    if (ks > 16) ks = 16;
-    if (ks > nblk) ks = nblk > 0 ? nblk : 1;
-    if (ks < 1) ks = 1;
-    c.KW = ks >= 2 ? 2 : 1;
-    c.S = (ks + c.KW - 1) / c.KW;
-    if (c.S > 8) c.S = 8;
-    while (c.S * c.KW > (nblk > 0 ? nblk : 1) && (c.S > 1 || c.KW > 1)) {
-        if (c.S > 1) --c.S; else --c.KW;
-    }
-    while (decode_smem_bytes(c, M, K) > 200 * 1024 && c.S < 8) ++c.S;
+    (void)dtype;
+    DecodeCfg c{1, 4, 4, 4, 1};   // R, NW, NB, NS, S
+    const int nblk = (K + kBoxK - 1) / kBoxK;
+    const int rt = 16 * c.R * c.NW;
+    const int tiles = (N + rt - 1) / rt;
+    // enough CTAs for ~3 per SM, split K across a cluster when rows are few
+    int S = 1;
+    while (S < 8 && tiles * S < 3 * sm_count && nblk / (S * 2) >= 2) S *= 2;
+    c.S = S;
+    const int nb = (nblk + S - 1) / S;
+    if (c.NB > nb) c.NB = nb > 0 ? nb : 1;
+    while (!decode_cfg_valid(c, M, K, G, sym == 0) && c.NS > 2) --c.NS;
+    while (!decode_cfg_valid(c, M, K, G, sym == 0) && c.S < 8) c.S *= 2;
     return c;
 }
 
-template <int DT, bool ASYM, int R, int D>
-static cudaError_t launch_t(const DecodeParams &p, const DecodeCfg &c, size_t smem,
-                            cudaStream_t s, bool pdl, int grid) {
-    auto kern = decode_kernel<DT, ASYM, R, D>;
+template <int DT, bool ASYM, int R>
+static cudaError_t launch_t(const CUtensorMap &tw, const DecodeParams &p, const DecodeCfg &c,
+                            size_t smem, cudaStream_t s, bool pdl, int grid) {
+    auto kern = decode_kernel<DT, ASYM, R>;
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
-    cfg.blockDim = dim3(32 * c.RW * c.KW, 1, 1);
+    cfg.blockDim = dim3(32 * c.NW, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attrs[2];
@@ -367,49 +408,58 @@ static cudaError_t launch_t(const DecodeParams &p, const DecodeCfg &c, size_t sm
     }
     cfg.attrs = attrs;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, kern, p);
-}
-
-template <int DT, bool ASYM>
-static cudaError_t launch_rd(const DecodeParams &p, const DecodeCfg &c, size_t smem,
-                             cudaStream_t s, bool pdl, int grid) {
-    if (c.R == 1)
-        return c.D == 2 ? launch_t<DT, ASYM, 1, 2>(p, c, smem, s, pdl, grid)
-                        : launch_t<DT, ASYM, 1, 4>(p, c, smem, s, pdl, grid);
-    return c.D == 2 ? launch_t<DT, ASYM, 2, 2>(p, c, smem, s, pdl, grid)
-                    : launch_t<DT, ASYM, 2, 4>(p, c, smem, s, pdl, grid);
+    return cudaLaunchKernelEx(&cfg, kern, tw, p);
 }
 
 cudaError_t launch_decode(const GemmArgs &a, const DecodeCfg &c, const DeviceInfo &dev,
                           cudaStream_t s, bool pdl) {
-    (void)dev;
+    if (dev.encode_tiled == nullptr) return cudaErrorNotSupported;
+    const bool asym = a.qzeros != nullptr;
+    const int RT = 16 * c.R * c.NW;
+    CUtensorMap tw;
+    {
+        EncodeTiledFn encode = reinterpret_cast<EncodeTiledFn>(dev.encode_tiled);
+        cuuint64_t dims[2] = {(cuuint64_t)(a.K / 8), (cuuint64_t)a.N};
+        cuuint64_t strides[1] = {(cuuint64_t)(a.K / 8) * 4};
+        cuuint32_t box[2] = {(cuuint32_t)(kBoxK / 8), (cuuint32_t)RT};
+        cuuint32_t estr[2] = {1, 1};
+        CUresult r = encode(&tw, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<int32_t *>(a.qweight), dims,
+                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
     DecodeParams p;
     p.x = (const uint16_t *)a.x;
-    p.qw = a.qweight;
     p.scales = (const uint16_t *)a.scales;
     p.qz = a.qzeros;
     p.out = (uint16_t *)a.out;
+    p.status = dev.status;
     p.M = a.M;
     p.N = a.N;
     p.K = a.K;
     p.G = a.G;
     p.ng = a.K / a.G;
-    p.RW = c.RW;
-    p.KW = c.KW;
+    p.log2G = a.G == 32 ? 5 : (a.G == 64 ? 6 : 7);
+    p.NW = c.NW;
+    p.NB = c.NB;
+    p.NS = c.NS;
     p.S = c.S;
-    p.nblk = a.K / 128;
-    p.ntail = (a.K % 128) / 32;
-    p.xpitch = xpitch_bytes(c, a.K);
-    const int rows_cta = 16 * c.R * c.RW;
-    const int tiles = (a.N + rows_cta - 1) / rows_cta;
+    p.nblk = (a.K + kBoxK - 1) / kBoxK;
+    p.xpitch = decode_xpitch(c, a.K);
+    p.gmax = decode_gmax(c, a.K, a.G);
+    const int tiles = (a.N + RT - 1) / RT;
     const int grid = tiles * c.S;
-    const size_t smem = decode_smem_bytes(c, a.M, a.K);
-    const bool asym = a.qzeros != nullptr;
-    if (a.dtype == 0)
-        return asym ? launch_rd<0, true>(p, c, smem, s, pdl, grid)
-                    : launch_rd<0, false>(p, c, smem, s, pdl, grid);
-    return asym ? launch_rd<1, true>(p, c, smem, s, pdl, grid)
-                : launch_rd<1, false>(p, c, smem, s, pdl, grid);
+    const size_t smem = decode_smem_bytes(c, a.M, a.K, a.G, asym);
+    if (a.dtype == 0) {
+        if (asym) return c.R == 1 ? launch_t<0, true, 1>(tw, p, c, smem, s, pdl, grid)
+                                  : launch_t<0, true, 2>(tw, p, c, smem, s, pdl, grid);
+        return c.R == 1 ? launch_t<0, false, 1>(tw, p, c, smem, s, pdl, grid)
+                        : launch_t<0, false, 2>(tw, p, c, smem, s, pdl, grid);
+    }
+    if (asym) return c.R == 1 ? launch_t<1, true, 1>(tw, p, c, smem, s, pdl, grid)
+                              : launch_t<1, true, 2>(tw, p, c, smem, s, pdl, grid);
+    return c.R == 1 ? launch_t<1, false, 1>(tw, p, c, smem, s, pdl, grid)
+                    : launch_t<1, false, 2>(tw, p, c, smem, s, pdl, grid);
 }
 
 }  // namespace w4a16

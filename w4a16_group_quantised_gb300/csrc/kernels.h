@@ -33,24 +33,26 @@ cudaError_t launch_dequant(const int32_t *qweight, const void *scales, const int
 
 // ---- decode.cu
 struct DecodeCfg {
-    int R;    // 16-row blocks per warp
-    int D;    // pipeline depth (register ring of weight steps)
-    int RW;   // warps along rows in a CTA
-    int KW;   // warps along K in a CTA
+    int R;    // 16-row blocks per warp (1, 2)
+    int NW;   // warps per CTA (1, 2, 4, 8); a CTA owns 16 * R * NW rows
+    int NB;   // TMA boxes (128 k each) per ring stage (1..8)
+    int NS;   // ring stages (2..8)
     int S;    // CTAs along K in a cluster (1..8)
 };
 DecodeCfg decode_pick_cfg(int M, int N, int K, int G, int sym, int dtype, int sm_count);
-bool decode_cfg_valid(const DecodeCfg &c, int M, int K);
-size_t decode_smem_bytes(const DecodeCfg &c, int M, int K);
+bool decode_cfg_valid(const DecodeCfg &c, int M, int K, int G, bool asym);
+size_t decode_smem_bytes(const DecodeCfg &c, int M, int K, int G, bool asym);
 cudaError_t launch_decode(const GemmArgs &a, const DecodeCfg &c, const DeviceInfo &dev,
                           cudaStream_t s, bool pdl);
 
 // ---- prefill.cu
 struct PrefillCfg {
     int BN;       // tokens per tile (MMA N), multiple of 16, <= 256
-    int stages;   // TMA stages (x + raw weights)
-    int astages;  // dequantised-weight stages
+    int stages;   // x-tile ring stages (64 k each)
+    int astages;  // dequantised-weight ring stages
+    int wstages;  // packed-weight ring stages (256 k each)
 };
+bool prefill_cfg_valid(const PrefillCfg &c);
 PrefillCfg prefill_pick_cfg(int M, int N, int K, int G, int sym, int dtype, int sm_count);
 cudaError_t launch_prefill(const GemmArgs &a, const PrefillCfg &c, const DeviceInfo &dev,
                            cudaStream_t s, bool pdl);

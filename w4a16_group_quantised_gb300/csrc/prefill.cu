@@ -7,23 +7,27 @@
 // the same packed [N, K/8] weights.
 //
 // Design (GB300-first):
-//  * One CTA computes a 128 (weight rows n) x BN (tokens m) output tile.  The
-//    dequantised weights are the MMA's A operand (M = 128) and the
-//    activations the B operand (N = BN <= 256), so the costly operand (W,
-//    which must be dequantised by the SM's ALUs) is the smaller one per FLOP.
-//  * Warp 0: TMA producer.  Per 64-wide K step it loads the x tile (BN rows x
-//    128 B, 128-byte swizzle) and the packed weight tile (128 rows x 32 B)
-//    into a `stages`-deep ring, completion tracked by transaction bytes.
-//  * Warps 4..7: dequantisers (one weight row per thread).  They turn the
-//    packed tile into a bf16/fp16 tile in the canonical K-major 128-byte
-//    swizzled layout the tensor core reads, fence it into the async proxy and
-//    arrive on the A-ring barrier.  Scales and zero points are prefetched
-//    four steps ahead in registers.  After the main loop the same warps are
-//    the epilogue: tcgen05.ld from TMEM, round once to the output dtype,
-//    store (TMEM lane quadrant = warp % 4).
-//  * Warp 1: TMEM allocation and the single-thread MMA issuer
-//    (tcgen05.mma.cta_group::1.kind::f16, 128 x BN x 16 per instruction,
-//    fp32 accumulator in TMEM); tcgen05.commit releases ring slots.
+//  * One CTA computes a 256 (weight rows n) x BN (tokens m) output tile as
+//    two 128-row halves.  The dequantised weights are the MMA's A operand
+//    (M = 128 per half) and the activations the shared B operand (N = BN <=
+//    256): every x tile feeds 2 x 128 x BN MACs per k, which halves the
+//    L2 -> SM activation traffic per FLOP against a 128-row tile.
+//  * Warp 0: TMA producer.  Per 64-wide K step it loads the x tile (BN rows
+//    x 128 B, 128-byte swizzle) into an SX-deep ring; every 4 steps it loads
+//    the packed weights of those 256 k (256 rows x 128 B, 128-byte swizzle)
+//    into an SW-deep ring.
+//  * Warps 4..11: dequantisers, one weight row per thread.  Each turns its
+//    row's 32 packed bytes per step into 64 bf16/fp16 weights in the
+//    canonical K-major 128-byte-swizzled layout the tensor core reads, fences
+//    them into the async proxy, and each warp arrives once on the A-ring
+//    barrier.  Scales and zero points are prefetched four steps ahead in
+//    registers.  After the main loop the same warps are the epilogue:
+//    tcgen05.ld from TMEM (lane quadrant = warp % 4), one rounding to the
+//    output dtype, a [BN x 256] tile staged in shared memory, one TMA store.
+//  * Warp 1: TMEM allocation (512 columns: two fp32 accumulators) and the
+//    single-thread MMA issuer (tcgen05.mma.cta_group::1.kind::f16,
+//    128 x BN x 16 per instruction, two per 16 k); tcgen05.commit releases
+//    ring slots and finally signals the epilogue.
 //  * Every mbarrier wait is bounded (%globaltimer); a wait that runs out sets
 //    the device status word and a CTA abort flag, and every role leaves its
 //    loop, so the CTA still frees its TMEM and exits.
@@ -35,21 +39,23 @@
 
 namespace w4a16 {
 
-constexpr int kBM = 128;          // weight rows per tile (MMA M)
-constexpr int kBK = 64;           // K per pipeline step (one 128-byte swizzle row of 16-bit)
-constexpr int kThreads = 256;
-constexpr int kATileBytes = kBM * kBK * 2;   // 16 KB
-constexpr int kWTileBytes = kBM * kBK / 2;   // 4 KB packed
+constexpr int kHalf = 128;                     // rows per MMA (M)
+constexpr int kBW = 2 * kHalf;                 // weight rows per CTA
+constexpr int kBK = 64;                        // k per MMA step
+constexpr int kWK = 256;                       // k per packed-weight stage (128 B a row)
+constexpr int kStepsPerW = kWK / kBK;          // 4
+constexpr int kThreads = 384;                  // 12 warps
+constexpr int kDeqWarps = 8;
+constexpr int kATileBytes = kBW * kBK * 2;     // 32 KB: both halves
+constexpr int kWTileBytes = kBW * kWK / 2;     // 32 KB packed
 constexpr int kScalePrefetch = 4;
 
 struct PrefillParams {
     const uint16_t *scales;
     const int32_t *qz;
-    uint16_t *out;
     int M, N, K, G, ng;
-    int BN, stages, astages;
+    int BN, SX, SA, SW;
     int n_mtiles;
-    int tmem_cols;
     int *status;
 };
 
@@ -68,46 +74,53 @@ struct SmemLayout {
     uint32_t x_off, a_off, w_off, bar_off, total;
 };
 
-__host__ __device__ inline SmemLayout prefill_layout(int BN, int stages, int astages) {
+__host__ __device__ inline SmemLayout prefill_layout(int BN, int SX, int SA, int SW) {
     SmemLayout L;
     uint32_t off = 0;
     L.x_off = off;
-    off += (uint32_t)stages * BN * 128;
+    off += (uint32_t)SX * BN * 128;
     off = (off + 1023u) & ~1023u;
     L.a_off = off;
-    off += (uint32_t)astages * kATileBytes;
+    off += (uint32_t)SA * kATileBytes;
     L.w_off = off;
-    off += (uint32_t)stages * kWTileBytes;
+    off += (uint32_t)SW * kWTileBytes;
     L.bar_off = off;
-    off += (uint32_t)(2 * stages + 2 * astages + 1) * 8 + 16;
+    off += (uint32_t)(2 * SX + 2 * SA + 2 * SW + 1) * 8 + 16;
     L.total = off + 1024;  // slack for aligning the dynamic base to 1024
     return L;
 }
 
+// The epilogue stages a [BN][256] output tile (512 B a row) over the x and A rings.
+__host__ __device__ inline bool prefill_epilogue_fits(int BN, int SX, int SA) {
+    return (uint32_t)BN * kBW * 2 <= (uint32_t)SX * BN * 128 + (uint32_t)SA * kATileBytes;
+}
+
 template <int DT, bool ASYM>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap tmap_x,
-                   const __grid_constant__ CUtensorMap tmap_w, const PrefillParams p) {
+    prefill_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
+                   const __grid_constant__ CUtensorMap tmap_out, const PrefillParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    const SmemLayout L = prefill_layout(p.BN, p.stages, p.astages);
+    const SmemLayout L = prefill_layout(p.BN, p.SX, p.SA, p.SW);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int stages = p.stages, astages = p.astages;
+    const int SX = p.SX, SA = p.SA, SW = p.SW;
 
     const int mt = blockIdx.x % p.n_mtiles;
     const int nt = blockIdx.x / p.n_mtiles;
-    const int m0 = mt * p.BN, n0 = nt * kBM;
+    const int m0 = mt * p.BN, n0 = nt * kBW;
     const int nk = (p.K + kBK - 1) / kBK;
 
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar_off);
-    const uint32_t bar_base = smem_u32(bars);
-    auto full_bar = [&](int s) { return bar_base + 8u * s; };
-    auto empty_bar = [&](int s) { return bar_base + 8u * (stages + s); };
-    auto afull_bar = [&](int a) { return bar_base + 8u * (2 * stages + a); };
-    auto aempty_bar = [&](int a) { return bar_base + 8u * (2 * stages + astages + a); };
-    const uint32_t acc_bar = bar_base + 8u * (2 * stages + 2 * astages);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.bar_off + 8 * (2 * stages + 2 * astages + 1));
+    const uint32_t bar_base = smem_u32(smem + L.bar_off);
+    auto xfull = [&](int s) { return bar_base + 8u * s; };
+    auto xempty = [&](int s) { return bar_base + 8u * (SX + s); };
+    auto afull = [&](int a) { return bar_base + 8u * (2 * SX + a); };
+    auto aempty = [&](int a) { return bar_base + 8u * (2 * SX + SA + a); };
+    auto wfull = [&](int w) { return bar_base + 8u * (2 * SX + 2 * SA + w); };
+    auto wempty = [&](int w) { return bar_base + 8u * (2 * SX + 2 * SA + SW + w); };
+    const uint32_t acc_bar = bar_base + 8u * (2 * SX + 2 * SA + 2 * SW);
+    uint32_t *tmem_slot =
+        reinterpret_cast<uint32_t *>(smem + L.bar_off + 8 * (2 * SX + 2 * SA + 2 * SW + 1));
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const uint32_t x_base = smem_u32(smem + L.x_off);
@@ -115,13 +128,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t w_base = smem_u32(smem + L.w_off);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < stages; ++s) {
-            mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 128 + 1);
+        for (int s = 0; s < SX; ++s) {
+            mbar_init(xfull(s), 1);
+            mbar_init(xempty(s), 1);             // MMA commit
         }
-        for (int a = 0; a < astages; ++a) {
-            mbar_init(afull_bar(a), 128);
-            mbar_init(aempty_bar(a), 1);
+        for (int a = 0; a < SA; ++a) {
+            mbar_init(afull(a), kDeqWarps);      // one arrive per dequant warp
+            mbar_init(aempty(a), 1);             // MMA commit
+        }
+        for (int w = 0; w < SW; ++w) {
+            mbar_init(wfull(w), 1);
+            mbar_init(wempty(w), kDeqWarps);
         }
         mbar_init(acc_bar, 1);
         *abort_flag = 0;
@@ -130,9 +147,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmap_x);
         tma_prefetch_desc(&tmap_w);
+        tma_prefetch_desc(&tmap_out);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), (uint32_t)p.tmem_cols);
+        tmem_alloc(smem_u32(tmem_slot), 512u);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -146,45 +164,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             grid_dependency_wait();  // x may be written by the previous kernel
-            const uint32_t tx = (uint32_t)p.BN * 128u + (uint32_t)kWTileBytes;
+            const uint32_t xtx = (uint32_t)p.BN * 128u;
             for (int i = 0; i < nk; ++i) {
-                const int s = i % stages;
-                const uint32_t ph = (uint32_t)((i / stages) & 1);
-                if (!mbar_wait_bounded(empty_bar(s), ph ^ 1u, p.status, abort_flag)) break;
-                mbar_arrive_expect_tx(full_bar(s), tx);
-                tma_load_2d(x_base + (uint32_t)s * p.BN * 128u, &tmap_x, full_bar(s), i * kBK, m0);
-                tma_load_2d(w_base + (uint32_t)s * kWTileBytes, &tmap_w, full_bar(s), i * (kBK / 8), n0);
+                if (i % kStepsPerW == 0) {
+                    const int j = i / kStepsPerW, sw = j % SW;
+                    if (!mbar_wait_bounded(wempty(sw), (uint32_t)((j / SW) & 1) ^ 1u, p.status, abort_flag))
+                        break;
+                    mbar_arrive_expect_tx(wfull(sw), (uint32_t)kWTileBytes);
+                    tma_load_2d(w_base + (uint32_t)sw * kWTileBytes, &tmap_w, wfull(sw), j * (kWK / 8), n0);
+                }
+                const int s = i % SX;
+                if (!mbar_wait_bounded(xempty(s), (uint32_t)((i / SX) & 1) ^ 1u, p.status, abort_flag)) break;
+                mbar_arrive_expect_tx(xfull(s), xtx);
+                tma_load_2d(x_base + (uint32_t)s * p.BN * 128u, &tmap_x, xfull(s), i * kBK, m0);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = make_idesc_f16(DT, kBM, p.BN);
+            const uint32_t idesc = make_idesc_f16(DT, kHalf, p.BN);
             for (int i = 0; i < nk; ++i) {
-                const int s = i % stages, a = i % astages;
-                if (!mbar_wait_bounded(full_bar(s), (uint32_t)((i / stages) & 1), p.status, abort_flag)) break;
-                if (!mbar_wait_bounded(afull_bar(a), (uint32_t)((i / astages) & 1), p.status, abort_flag)) break;
+                const int s = i % SX, a = i % SA;
+                if (!mbar_wait_bounded(xfull(s), (uint32_t)((i / SX) & 1), p.status, abort_flag)) break;
+                if (!mbar_wait_bounded(afull(a), (uint32_t)((i / SA) & 1), p.status, abort_flag)) break;
                 tc_fence_after();
                 const uint32_t xa = x_base + (uint32_t)s * p.BN * 128u;
                 const uint32_t aa = a_base + (uint32_t)a * kATileBytes;
 #pragma unroll
                 for (int kk = 0; kk < kBK / 16; ++kk) {
-                    tc_mma_f16(tmem_d, smem_desc_sw128(aa + kk * 32), smem_desc_sw128(xa + kk * 32),
-                               idesc, (i > 0 || kk > 0) ? 1u : 0u);
+                    const uint64_t bdesc = smem_desc_sw128(xa + kk * 32);
+                    const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                    tc_mma_f16(tmem_d, smem_desc_sw128(aa + kk * 32), bdesc, idesc, acc);
+                    tc_mma_f16(tmem_d + 256u, smem_desc_sw128(aa + kHalf * 128 + kk * 32), bdesc, idesc, acc);
                 }
-                tc_commit(empty_bar(s));
-                tc_commit(aempty_bar(a));
+                tc_commit(xempty(s));
+                tc_commit(aempty(a));
             }
             tc_commit(acc_bar);
         }
         __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------------------------------ dequantisers
-        const int r = threadIdx.x - 128;          // weight row within the tile
+        const int r = threadIdx.x - 128;               // weight row within the tile, 0..255
         const int n = n0 + r;
         const bool vrow = n < p.N;
         const int zshift = 4 * (n & 7);
-        // scale / zero-point register ring: [slot] = (lo-half group, hi-half group)
         uint32_t rs_lo[kScalePrefetch], rs_hi[kScalePrefetch], rz_lo[kScalePrefetch], rz_hi[kScalePrefetch];
         auto load_meta = [&](int i, uint32_t &slo, uint32_t &shi, uint32_t &zlo, uint32_t &zhi) {
             slo = shi = 0u;
@@ -203,8 +227,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int d = 0; d < kScalePrefetch; ++d) load_meta(d, rs_lo[d], rs_hi[d], rz_lo[d], rz_hi[d]);
 
-        const uint32_t a_row = (uint32_t)(r >> 3) * 1024u + (uint32_t)(r & 7) * 128u;
+        // A tile (both halves): half h = r / 128 at h * 16 KB; 128-byte rows,
+        // 16-byte chunk c of row r at position c ^ (r % 8) within its 8-row atom.
         const uint32_t sw = (uint32_t)(r & 7);
+        const uint32_t a_row = (uint32_t)(r >> 7) * (kHalf * 128) + (uint32_t)((r & 127) >> 3) * 1024u +
+                               sw * 128u;
+        const uint32_t w_row = (uint32_t)(r >> 3) * 1024u + sw * 128u;   // packed tile, same swizzle
         bool ok = true;
         for (int i0 = 0; i0 < nk && ok; i0 += kScalePrefetch) {
 #pragma unroll
@@ -219,17 +247,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     load_meta(i + kScalePrefetch, rs_lo[d], rs_hi[d], rz_lo[d], rz_hi[d]);
 
-                    const int s = i % stages, a = i % astages;
-                    if (!mbar_wait_bounded(full_bar(s), (uint32_t)((i / stages) & 1), p.status, abort_flag)) {
+                    const int j = i / kStepsPerW, jj = i % kStepsPerW, swi = j % SW;
+                    if (jj == 0 &&
+                        !mbar_wait_bounded(wfull(swi), (uint32_t)((j / SW) & 1), p.status, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    const unsigned char *wsrc = smem + L.w_off + (size_t)s * kWTileBytes + (size_t)r * 32;
-                    const uint4 w0 = *reinterpret_cast<const uint4 *>(wsrc);
-                    const uint4 w1 = *reinterpret_cast<const uint4 *>(wsrc + 16);
-                    mbar_arrive(empty_bar(s));
-                    if (!mbar_wait_bounded(aempty_bar(a), (uint32_t)((i / astages) & 1) ^ 1u, p.status,
-                                           abort_flag)) {
+                    const unsigned char *wrow = smem + L.w_off + (size_t)swi * kWTileBytes + w_row;
+                    const uint4 w0 = *reinterpret_cast<const uint4 *>(wrow + (((uint32_t)(2 * jj) ^ sw) << 4));
+                    const uint4 w1 = *reinterpret_cast<const uint4 *>(wrow + (((uint32_t)(2 * jj + 1) ^ sw) << 4));
+                    if (jj == kStepsPerW - 1 || i == nk - 1) {
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(wempty(swi));
+                    }
+                    const int a = i % SA;
+                    if (!mbar_wait_bounded(aempty(a), (uint32_t)((i / SA) & 1) ^ 1u, p.status, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -244,29 +276,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                         *reinterpret_cast<uint4 *>(adst + (((uint32_t)c ^ sw) << 4)) =
                             make_uint4(o[0], o[1], o[2], o[3]);
                     }
-                    fence_proxy_async_smem();
-                    mbar_arrive(afull_bar(a));
+                    fence_proxy_async_smem();   // each writer: generic -> async proxy
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(afull(a));
                 }
             }
         }
 
         // ------------------------------------------------------------ epilogue
-        if (ok && mbar_wait_bounded(acc_bar, 0u, p.status, abort_flag)) {
+        const bool have_acc = ok && mbar_wait_bounded(acc_bar, 0u, p.status, abort_flag);
+        if (have_acc) {
             tc_fence_after();
-            const int q = warp & 3;
-            const int nrow = n0 + 32 * q + lane;
-            const uint32_t tbase = tmem_d + ((uint32_t)(32 * q) << 16);
+            const int q = warp & 3, h = (warp - 4) >> 2;
+            const int nl = h * kHalf + 32 * q + lane;            // row of the tile
+            const uint32_t tbase = tmem_d + ((uint32_t)(32 * q) << 16) + (uint32_t)(h * 256);
+            uint16_t *stage = reinterpret_cast<uint16_t *>(smem);   // [BN][256], over x/A rings
             for (int c0 = 0; c0 < p.BN; c0 += 16) {
                 uint32_t v[16];
                 tmem_ld_32x32b_x16(tbase + (uint32_t)c0, v);
-                if (nrow < p.N) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int m = m0 + c0 + j;
-                        if (m < p.M) p.out[(size_t)m * p.N + nrow] = f32_to_dt16<DT>(__uint_as_float(v[j]));
-                    }
-                }
+                for (int jx = 0; jx < 16; ++jx)
+                    stage[(size_t)(c0 + jx) * kBW + nl] = f32_to_dt16<DT>(__uint_as_float(v[jx]));
             }
+            fence_proxy_async_smem();
+        }
+        named_barrier_sync(1, kDeqWarps * 32);
+        if (have_acc && threadIdx.x == 128) {
+            tma_store_2d(&tmap_out, smem_u32(smem), n0, m0);
+            bulk_commit_group();
+            bulk_wait_group_all();
         }
     }
 
@@ -274,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_d, (uint32_t)p.tmem_cols);
+        tmem_dealloc(tmem_d, 512u);
     }
 }
 
@@ -284,25 +322,50 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+static bool prefill_cfg_fits(const PrefillCfg &c) {
+    return prefill_layout(c.BN, c.stages, c.astages, c.wstages).total <= 227 * 1024 &&
+           prefill_epilogue_fits(c.BN, c.stages, c.astages);
+}
+
+// Pick BN (tokens per tile) to minimise waves x tile time on the SMs, then
+// the deepest x ring that fits.
 PrefillCfg prefill_pick_cfg(int M, int N, int K, int G, int sym, int dtype, int sm_count) {
-    (void)N; (void)K; (void)G; (void)sym; (void)dtype; (void)sm_count;
-    PrefillCfg c;
-    const int tiles_m = (M + 255) / 256;
-    int bn = (M + tiles_m - 1) / tiles_m;
-    bn = ((bn + 15) / 16) * 16;
-    if (bn < 16) bn = 16;
-    if (bn > 256) bn = 256;
-    c.BN = bn;
-    c.astages = 3;
-    c.stages = 4;
-    // keep within 227 KB: x ring dominates for large BN
-    while (c.stages > 2 && prefill_layout(c.BN, c.stages, c.astages).total > 227 * 1024) --c.stages;
+    (void)K; (void)G; (void)sym; (void)dtype;
+    const int ntiles_n = (N + kBW - 1) / kBW;
+    int best_bn = 256;
+    double best_cost = 1e30;
+    for (int bn = 256; bn >= 64; bn -= 16) {
+        const int mt = (M + bn - 1) / bn;
+        const long long tiles = (long long)mt * ntiles_n;
+        const long long waves = (tiles + sm_count - 1) / sm_count;
+        // per-tile time ~ bn (tensor-bound) + a fixed part for dequant/pipeline
+        const double cost = (double)waves * (bn + 48);
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best_bn = bn;
+        }
+    }
+    PrefillCfg c{best_bn, 3, 2, 2};
+    if (M < best_bn) {
+        c.BN = ((M + 15) / 16) * 16;
+        if (c.BN < 16) c.BN = 16;
+    }
+    for (int sx = 6; sx >= 2; --sx) {
+        c.stages = sx;
+        if (prefill_cfg_fits(c)) break;
+    }
     return c;
 }
 
+bool prefill_cfg_valid(const PrefillCfg &c) {
+    if (c.BN < 16 || c.BN > 256 || c.BN % 16 != 0) return false;
+    if (c.stages < 2 || c.astages < 2 || c.wstages < 2) return false;
+    return prefill_cfg_fits(c);
+}
+
 template <int DT, bool ASYM>
-static cudaError_t launch_t(const CUtensorMap &tx, const CUtensorMap &tw, const PrefillParams &p,
-                            size_t smem, int grid, cudaStream_t s, bool pdl) {
+static cudaError_t launch_t(const CUtensorMap &tx, const CUtensorMap &tw, const CUtensorMap &to,
+                            const PrefillParams &p, size_t smem, int grid, cudaStream_t s, bool pdl) {
     auto kern = prefill_kernel<DT, ASYM>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -320,7 +383,7 @@ static cudaError_t launch_t(const CUtensorMap &tx, const CUtensorMap &tw, const 
     }
     cfg.attrs = attrs;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, kern, tx, tw, p);
+    return cudaLaunchKernelEx(&cfg, kern, tx, tw, to, p);
 }
 
 cudaError_t prefill_prepare_device(const DeviceInfo &dev) {
@@ -331,55 +394,64 @@ cudaError_t prefill_prepare_device(const DeviceInfo &dev) {
 cudaError_t launch_prefill(const GemmArgs &a, const PrefillCfg &c, const DeviceInfo &dev,
                            cudaStream_t s, bool pdl) {
     if (dev.encode_tiled == nullptr) return cudaErrorNotSupported;
+    if (!prefill_cfg_valid(c)) return cudaErrorInvalidValue;
     EncodeTiledFn encode = reinterpret_cast<EncodeTiledFn>(dev.encode_tiled);
-    CUtensorMap tx, tw;
+    const CUtensorMapDataType act = a.dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUtensorMap tx, tw, to;
     {
         cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
         cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
         cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)c.BN};
         cuuint32_t estr[2] = {1, 1};
-        CUresult r = encode(&tx, a.dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                            2, const_cast<void *>(a.x), dims, strides, box, estr,
-                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+        if (encode(&tx, act, 2, const_cast<void *>(a.x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
     }
     {
         cuuint64_t dims[2] = {(cuuint64_t)(a.K / 8), (cuuint64_t)a.N};
         cuuint64_t strides[1] = {(cuuint64_t)(a.K / 8) * 4};
-        cuuint32_t box[2] = {(cuuint32_t)(kBK / 8), (cuuint32_t)kBM};
+        cuuint32_t box[2] = {(cuuint32_t)(kWK / 8), (cuuint32_t)kBW};
         cuuint32_t estr[2] = {1, 1};
-        CUresult r = encode(&tw, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<int32_t *>(a.qweight), dims,
-                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+        if (encode(&tw, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<int32_t *>(a.qweight), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)a.N, (cuuint64_t)a.M};
+        cuuint64_t strides[1] = {(cuuint64_t)a.N * 2};
+        cuuint32_t box[2] = {(cuuint32_t)kBW, (cuuint32_t)c.BN};
+        cuuint32_t estr[2] = {1, 1};
+        if (encode(&to, act, 2, a.out, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
     }
     PrefillParams p;
     p.scales = (const uint16_t *)a.scales;
     p.qz = a.qzeros;
-    p.out = (uint16_t *)a.out;
     p.M = a.M;
     p.N = a.N;
     p.K = a.K;
     p.G = a.G;
     p.ng = a.K / a.G;
     p.BN = c.BN;
-    p.stages = c.stages;
-    p.astages = c.astages;
+    p.SX = c.stages;
+    p.SA = c.astages;
+    p.SW = c.wstages;
     p.n_mtiles = (a.M + c.BN - 1) / c.BN;
-    int cols = 32;
-    while (cols < c.BN) cols <<= 1;
-    p.tmem_cols = cols;
     p.status = dev.status;
-    const int n_ntiles = (a.N + kBM - 1) / kBM;
+    const int n_ntiles = (a.N + kBW - 1) / kBW;
     const int grid = n_ntiles * p.n_mtiles;
-    const size_t smem = prefill_layout(c.BN, c.stages, c.astages).total;
+    const size_t smem = prefill_layout(c.BN, c.stages, c.astages, c.wstages).total;
     const bool asym = a.qzeros != nullptr;
     if (a.dtype == 0)
-        return asym ? launch_t<0, true>(tx, tw, p, smem, grid, s, pdl)
-                    : launch_t<0, false>(tx, tw, p, smem, grid, s, pdl);
-    return asym ? launch_t<1, true>(tx, tw, p, smem, grid, s, pdl)
-                : launch_t<1, false>(tx, tw, p, smem, grid, s, pdl);
+        return asym ? launch_t<0, true>(tx, tw, to, p, smem, grid, s, pdl)
+                    : launch_t<0, false>(tx, tw, to, p, smem, grid, s, pdl);
+    return asym ? launch_t<1, true>(tx, tw, to, p, smem, grid, s, pdl)
+                : launch_t<1, false>(tx, tw, to, p, smem, grid, s, pdl);
 }
 
 }  // namespace w4a16
