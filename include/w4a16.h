@@ -72,6 +72,12 @@ typedef enum {
     W4A16_ERR_ARG = -9       /* other invalid argument (e.g. path enum)       */
 } w4a16_status_t;
 
+/* Concurrency: the skinny decode kernel keeps per-row-block tickets and
+ * partial sums in a workspace owned by the library (one per device, made by
+ * the first call on that device).  Decode-path calls on one device must
+ * therefore not run concurrently on different streams; calls on one stream
+ * (the usual case, with or without CUDA graphs) are always safe. */
+
 /* Limits checked by the validation (shapes must also fit in int32 indexing). */
 #define W4A16_MAX_DECODE_M 8
 
@@ -153,7 +159,9 @@ int w4a16_version(void);
  * which = 2: prefill configuration vals = {BN, x-ring stages, dequantised-
  * weight stages, packed-weight stages}, n = 4 (BN a multiple of 16 in
  * [16, 256]; the rings must fit in shared memory);
- * which = 3: programmatic dependent launch on/off, vals = {flag}, n = 1.
+ * which = 3: programmatic dependent launch on/off, vals = {flag}, n = 1;
+ * which = 4: balanced decode kernel vals = {on (1) / off (0), load ring
+ * depth in units (2, 4 or 6)}, n = 2.
  * n = 0 restores the built-in choice for which = 1 or 2.  An invalid
  * configuration is rejected here or, for the decode shape limits, by the
  * next w4a16_gemm call with W4A16_ERR_ARG. */

@@ -39,6 +39,9 @@ DecodeCfg g_decode_cfg{};
 bool g_prefill_override = false;
 PrefillCfg g_prefill_cfg{};
 int g_pdl = 1;
+// balanced decode kernel: enabled flag and preferred ring depth
+int g_sk_on = 0, g_sk_ns = 4;
+constexpr int kSkMaxRowBlocks = 1 << 16;   // N up to 1M rows
 
 void init_device(DevState &st, int dev) {
     DeviceInfo &d = st.info;
@@ -77,6 +80,19 @@ void init_device(DevState &st, int dev) {
     if (prefill_prepare_device(d) != cudaSuccess) {
         st.rc = W4A16_ERR_CUDA;
         return;
+    }
+    // Workspace of the balanced decode kernel (allocated once per device,
+    // here, so that later calls never allocate).
+    {
+        const size_t wsf = decode_sk_workspace_floats(d.sm_count);
+        if (cudaMalloc(&d.sk_ws, wsf * sizeof(float)) != cudaSuccess ||
+            cudaMalloc(&d.sk_counters, sizeof(int) * kSkMaxRowBlocks) != cudaSuccess ||
+            cudaMemset(d.sk_counters, 0, sizeof(int) * kSkMaxRowBlocks) != cudaSuccess ||
+            cudaDeviceSynchronize() != cudaSuccess) {
+            st.rc = W4A16_ERR_CUDA;
+            return;
+        }
+        d.sk_max_rowblocks = kSkMaxRowBlocks;
     }
     const char *e = std::getenv("W4A16_PDL");
     if (e && e[0] == '0') g_pdl = 0;
@@ -148,6 +164,19 @@ int run_gemm(const void *x, int M, int K, const int32_t *qw, const void *scales,
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (path == W4A16_PATH_DECODE) {
+        int sk_on, ns_pref;
+        bool use_cluster_override;
+        {
+            std::lock_guard<std::mutex> lk(g_cfg_mu);
+            sk_on = g_sk_on;
+            ns_pref = g_sk_ns;
+            use_cluster_override = g_decode_override;
+        }
+        if (!use_cluster_override && sk_on && (N + 15) / 16 <= dev->sk_max_rowblocks &&
+            decode_sk_applicable(M, K)) {
+            e = launch_decode_sk(a, ns_pref, *dev, dev->sk_ws, dev->sk_counters, s, g_pdl != 0);
+            return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
+        }
         DecodeCfg c;
         {
             std::lock_guard<std::mutex> lk(g_cfg_mu);
@@ -313,6 +342,15 @@ int w4a16_debug_set_config(int which, const int *vals, int n) {
     if (which == 3) {
         if (n != 1 || vals == nullptr) return W4A16_ERR_ARG;
         g_pdl = vals[0] != 0;
+        return W4A16_OK;
+    }
+    if (which == 4) {
+        if (n == 0) { g_sk_on = 0; g_sk_ns = 4; return W4A16_OK; }
+        if (n != 2 || vals == nullptr) return W4A16_ERR_ARG;
+        if (vals[0] < 0 || vals[0] > 1 || (vals[1] != 2 && vals[1] != 4 && vals[1] != 6))
+            return W4A16_ERR_ARG;
+        g_sk_on = vals[0];
+        g_sk_ns = vals[1];
         return W4A16_OK;
     }
     return W4A16_ERR_ARG;

@@ -99,10 +99,19 @@ __device__ __forceinline__ void mac_word(float (&acc)[4], uint32_t wa, uint32_t 
     mma_16816<DT>(acc, oa[2], ob[2], oa[3], ob[3], xv.z, xv.w);
 }
 
+// zhi2 from zlo2: the same zero point moved from the low-magic to the
+// high-magic position in both lanes.
+template <int DT>
+__device__ __forceinline__ uint32_t zhi_from_zlo(uint32_t zl2) {
+    return ((zl2 & 0x000F000Fu) << (DT == 0 ? 4 : 3)) | rep2(Dtype<DT>::kMagicHi);
+}
+
 struct DecodeSmem {
-    uint32_t ring, scales, zeros, x, red, bars, total;
+    uint32_t ring, meta, x, red, bars, total;
 };
 
+// meta: per (row, group) of the slice, {s2} (symmetric) or {s2, zl2}
+// (asymmetric) -- the packed scale and low-magic zero constant, built once.
 __host__ __device__ inline DecodeSmem decode_layout(int R, int NW, int NB, int NS, int M, int xpitch,
                                                     int gmax, bool asym) {
     const int RT = 16 * R * NW;
@@ -110,23 +119,20 @@ __host__ __device__ inline DecodeSmem decode_layout(int R, int NW, int NB, int N
     uint32_t off = 0;
     L.ring = off;                                   // 128-B aligned for TMA
     off += (uint32_t)NS * NB * RT * kBoxRowBytes;
-    L.scales = off;                                 // [RT][gmax] uint16
-    off += (uint32_t)RT * gmax * 2;
-    off = (off + 15u) & ~15u;
-    L.zeros = off;                                  // [RT/8][gmax] uint32
-    off += asym ? (uint32_t)(RT / 8) * gmax * 4 : 0u;
+    L.meta = off;
+    off += (uint32_t)RT * gmax * (asym ? 8 : 4);
     off = (off + 127u) & ~127u;
     L.x = off;                                      // [M][xpitch]
     off += (uint32_t)M * xpitch;
-    L.red = off;                                    // [NW*R][16][8] fp32
-    off += (uint32_t)NW * R * 16 * 8 * 4;
+    L.red = off;                                    // [RT][8] fp32
+    off += (uint32_t)RT * 8 * 4;
     L.bars = off;
     off += (uint32_t)2 * NS * 8 + 16;
     L.total = off + 128;                            // slack to align the base to 128
     return L;
 }
 
-template <int DT, bool ASYM, int R>
+template <int DT, bool ASYM, int R, int NB>
 __global__ void __launch_bounds__(256) decode_kernel(const __grid_constant__ CUtensorMap tmap_w,
                                                      const DecodeParams p) {
     extern __shared__ unsigned char smem_raw[];
@@ -134,12 +140,13 @@ __global__ void __launch_bounds__(256) decode_kernel(const __grid_constant__ CUt
         (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~(uintptr_t)127);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
-    const int NW = p.NW, NB = p.NB, NS = p.NS, S = p.S;
+    const int NW = p.NW, NS = p.NS, S = p.S;
     const int RT = 16 * R * NW;
     const int rank = (S > 1) ? (int)cg::this_cluster().block_rank() : 0;
     const int tile = blockIdx.x / S;
     const int n_tile0 = tile * RT;
-    const DecodeSmem L = decode_layout(R, NW, NB, NS, p.M, p.xpitch, p.gmax, ASYM);
+    const int M = p.M, K = p.K, gmax = p.gmax, log2G = p.log2G;
+    const DecodeSmem L = decode_layout(R, NW, NB, NS, M, p.xpitch, gmax, ASYM);
 
     grid_dependents_launch();
 
@@ -148,32 +155,31 @@ __global__ void __launch_bounds__(256) decode_kernel(const __grid_constant__ CUt
     const int b1 = (int)((long long)(rank + 1) * p.nblk / S);
     const int nb = b1 - b0;
     const int nsteps = (nb + NB - 1) / NB;          // ring stages to consume
-    const int g0 = (b0 * kBoxK) / p.G;              // first group of the slice
-    const int g1 = min(p.ng, (b1 * kBoxK + p.G - 1) / p.G);
+    const int g0 = (b0 * kBoxK) >> log2G;           // first group of the slice
+    const int g1 = min(p.ng, (b1 * kBoxK + p.G - 1) >> log2G);
     const int ngs = g1 - g0;
 
-    const uint32_t ring = smem_u32(smem + L.ring);
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t ring = sbase + L.ring;
     const uint32_t stage_bytes = (uint32_t)NB * RT * kBoxRowBytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
-    const uint32_t bar0 = smem_u32(bars);
-    auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (NS + s); };
+    const uint32_t bar0 = sbase + L.bars;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.bars + 16 * NS);
 
     auto issue = [&](int step) {  // one thread: TMA all boxes of a ring stage
-        const int s = step % NS;
+        const uint32_t sfull = bar0 + 8u * (uint32_t)(step % NS);
+        const uint32_t sdst = ring + (uint32_t)(step % NS) * stage_bytes;
         const int bb = b0 + step * NB;
         const int nbox = min(NB, b1 - bb);
-        mbar_arrive_expect_tx(full_bar(s), (uint32_t)nbox * RT * kBoxRowBytes);
+        mbar_arrive_expect_tx(sfull, (uint32_t)nbox * RT * kBoxRowBytes);
         for (int j = 0; j < nbox; ++j)
-            tma_load_2d(ring + (uint32_t)s * stage_bytes + (uint32_t)j * RT * kBoxRowBytes, &tmap_w,
-                        full_bar(s), (bb + j) * (kBoxK / 8), n_tile0);
+            tma_load_2d(sdst + (uint32_t)j * RT * kBoxRowBytes, &tmap_w, sfull, (bb + j) * (kBoxK / 8),
+                        n_tile0);
     };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
-            mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), NW);
+            mbar_init(bar0 + 8u * s, 1);               // full
+            mbar_init(bar0 + 8u * (NS + s), NW);       // empty: one arrive per warp
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -181,33 +187,35 @@ __global__ void __launch_bounds__(256) decode_kernel(const __grid_constant__ CUt
         for (int st = 0; st < min(NS, nsteps); ++st) issue(st);
     }
 
-    // ---- scales and zero points of the slice (static: before the dependency wait)
-    uint16_t *s_sc = reinterpret_cast<uint16_t *>(smem + L.scales);
+    // ---- per-(row, group) constants of the slice (static: before the dependency wait)
     for (int i = threadIdx.x; i < RT * ngs; i += blockDim.x) {
-        const int r = i / ngs, gg = i % ngs;
+        const int r = i / ngs, gg = i - (i / ngs) * ngs;
         const int n = n_tile0 + r;
-        s_sc[r * p.gmax + gg] = n < p.N ? __ldg(p.scales + (size_t)n * p.ng + g0 + gg) : (uint16_t)0;
-    }
-    if (ASYM) {
-        uint32_t *s_z = reinterpret_cast<uint32_t *>(smem + L.zeros);
-        for (int i = threadIdx.x; i < (RT / 8) * ngs; i += blockDim.x) {
-            const int r8 = i / ngs, gg = i % ngs;
-            const int n8 = n_tile0 / 8 + r8;
-            s_z[r8 * p.gmax + gg] = n8 < p.N / 8 ? (uint32_t)__ldg(p.qz + (size_t)n8 * p.ng + g0 + gg) : 0u;
+        uint32_t s2 = 0u, zl2 = zlo2<DT>(8u);
+        if (n < p.N) {
+            s2 = rep2(__ldg(p.scales + (size_t)n * p.ng + g0 + gg));
+            if (ASYM) {
+                const uint32_t zw = (uint32_t)__ldg(p.qz + (size_t)(n >> 3) * p.ng + g0 + gg);
+                zl2 = zlo2<DT>((zw >> (4 * (n & 7))) & 0xFu);
+            }
         }
+        if (ASYM)
+            *reinterpret_cast<uint2 *>(smem + L.meta + ((size_t)r * gmax + gg) * 8) = make_uint2(s2, zl2);
+        else
+            *reinterpret_cast<uint32_t *>(smem + L.meta + ((size_t)r * gmax + gg) * 4) = s2;
     }
 
-    // ---- x slice -> shared memory, permuted; zero beyond K and for k >= K
+    // ---- x slice -> shared memory, permuted; zero for k >= K
     grid_dependency_wait();
-    unsigned char *xs = smem + L.x;
     {
+        unsigned char *xs = smem + L.x;
         const int nch = nb * 16;                   // 16-byte chunks per row
         const int kbase = b0 * kBoxK;
-        for (int i = threadIdx.x; i < p.M * nch; i += blockDim.x) {
-            const int m = i / nch, c = i % nch;
+        for (int i = threadIdx.x; i < M * nch; i += blockDim.x) {
+            const int m = i / nch, c = i - (i / nch) * nch;
             const int k = kbase + 8 * c;
             uint4 v = make_uint4(0, 0, 0, 0);
-            if (k < p.K) v = *reinterpret_cast<const uint4 *>(p.x + (size_t)m * p.K + k);
+            if (k < K) v = *reinterpret_cast<const uint4 *>(p.x + (size_t)m * K + k);
             const int b = c >> 4, cc = c & 15;
             const int pos = b * 16 + (cc & 3) * 4 + (cc >> 2);   // chunk 4t+w stored at 4w+t
             uint4 o;
@@ -228,77 +236,80 @@ __global__ void __launch_bounds__(256) decode_kernel(const __grid_constant__ CUt
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[rb][e] = acc2[rb][e] = 0.f;
 
-    const bool has_x = g < p.M;
-    const unsigned char *xrow = xs + (size_t)g * p.xpitch;
-    const uint16_t *s_sc_c = s_sc;
-    const uint32_t *s_z = reinterpret_cast<const uint32_t *>(smem + L.zeros);
-    const int rloc0 = warp * R * 16 + g;            // row of rb = 0 within the tile
+    const bool has_x = g < M;
+    const uint32_t xrow = sbase + L.x + (uint32_t)(g * p.xpitch) + (uint32_t)t * 16u;
+    const uint32_t meta = sbase + L.meta;
+    const int rloc0 = warp * R * 16 + g;             // row of rb = 0 within the tile
+    const uint32_t zl_sym = zlo2<DT>(8u), zh_sym = zhi2<DT>(8u);
 
     bool ok = true;
+    int s = 0, ps = NS - 1;                  // ring slot of this step and of the previous one
+    uint32_t par = 0u, ppar = 1u;            // their phase parities
     for (int step = 0; step < nsteps && ok; ++step) {
-        const int s = step % NS;
         // refill the slot used one step ago, once every warp has left it
         if (threadIdx.x == 0 && step > 0 && step - 1 + NS < nsteps) {
-            const int ps = (step - 1) % NS;
-            if (mbar_wait_bounded(empty_bar(ps), (uint32_t)(((step - 1) / NS) & 1), p.status, abort_flag))
-                issue(step - 1 + NS);
+            if (mbar_wait_bounded(bar0 + 8u * (NS + ps), ppar, p.status, abort_flag)) issue(step - 1 + NS);
         }
-        if (!mbar_wait_bounded(full_bar(s), (uint32_t)((step / NS) & 1), p.status, abort_flag)) {
+        if (!mbar_wait_bounded(bar0 + 8u * s, par, p.status, abort_flag)) {
             ok = false;
             break;
         }
-        const unsigned char *stage = smem + L.ring + (size_t)s * stage_bytes;
-        const int nbox = min(NB, b1 - (b0 + step * NB));
-        for (int j = 0; j < nbox; ++j) {
-            const int lb = step * NB + j;                 // local block index
-            const int kb = (b0 + lb) * kBoxK;             // first k of the block
-            const int gl = ((kb + 32 * t) >> p.log2G) - g0;  // this lane's group, slice-local
-            const bool kin = kb + 32 * t < p.K;
-            uint4 xv[4];
+        const uint32_t stage = ring + (uint32_t)s * stage_bytes;
+        const int lb0 = step * NB;
 #pragma unroll
-            for (int w = 0; w < 4; ++w)
-                xv[w] = has_x ? *reinterpret_cast<const uint4 *>(xrow + (lb * 16 + 4 * w + t) * 16)
-                              : make_uint4(0, 0, 0, 0);
-            const unsigned char *box = stage + (size_t)j * RT * kBoxRowBytes;
+        for (int j = 0; j < NB; ++j) {
+            const int lb = lb0 + j;                   // slice-local block
+            if (lb < nb) {
+                const int kb = (b0 + lb) * kBoxK;
+                const int gl = min(((kb + 32 * t) >> log2G) - g0, ngs - 1);
+                uint4 xv[4];
 #pragma unroll
-            for (int rb = 0; rb < R; ++rb) {
-                const int ra = rloc0 + rb * 16, rbw = ra + 8;
-                const uint4 wa = *reinterpret_cast<const uint4 *>(box + ra * kBoxRowBytes + 16 * t);
-                const uint4 wb = *reinterpret_cast<const uint4 *>(box + rbw * kBoxRowBytes + 16 * t);
-                uint32_t sa = 0u, sb = 0u, zA = 8u, zB = 8u;
-                if (kin) {
-                    sa = s_sc_c[ra * p.gmax + gl];
-                    sb = s_sc_c[rbw * p.gmax + gl];
-                    if (ASYM) {
-                        zA = (s_z[(ra >> 3) * p.gmax + gl] >> (4 * g)) & 0xFu;
-                        zB = (s_z[(rbw >> 3) * p.gmax + gl] >> (4 * g)) & 0xFu;
-                    }
+                for (int w = 0; w < 4; ++w) {
+                    xv[w] = make_uint4(0, 0, 0, 0);
+                    if (has_x) xv[w] = lds128(xrow + (uint32_t)(lb * 16 + 4 * w) * 16u);
                 }
-                const uint32_t zla = zlo2<DT>(zA), zha = zhi2<DT>(zA), s2a = rep2(sa);
-                const uint32_t zlb = zlo2<DT>(zB), zhb = zhi2<DT>(zB), s2b = rep2(sb);
-                mac_word<DT>(acc[rb], wa.x, wb.x, zla, zha, s2a, zlb, zhb, s2b, xv[0]);
-                mac_word<DT>(acc2[rb], wa.y, wb.y, zla, zha, s2a, zlb, zhb, s2b, xv[1]);
-                mac_word<DT>(acc[rb], wa.z, wb.z, zla, zha, s2a, zlb, zhb, s2b, xv[2]);
-                mac_word<DT>(acc2[rb], wa.w, wb.w, zla, zha, s2a, zlb, zhb, s2b, xv[3]);
+                const uint32_t box = stage + (uint32_t)j * RT * kBoxRowBytes + (uint32_t)t * 16u;
+#pragma unroll
+                for (int rb = 0; rb < R; ++rb) {
+                    const int ra = rloc0 + rb * 16, rbw = ra + 8;
+                    const uint4 wa = lds128(box + (uint32_t)ra * kBoxRowBytes);
+                    const uint4 wb = lds128(box + (uint32_t)rbw * kBoxRowBytes);
+                    uint32_t s2a, s2b, zla = zl_sym, zlb = zl_sym, zha = zh_sym, zhb = zh_sym;
+                    if (ASYM) {
+                        const uint2 ma = lds64(meta + (uint32_t)(ra * gmax + gl) * 8u);
+                        const uint2 mb = lds64(meta + (uint32_t)(rbw * gmax + gl) * 8u);
+                        s2a = ma.x; zla = ma.y; zha = zhi_from_zlo<DT>(zla);
+                        s2b = mb.x; zlb = mb.y; zhb = zhi_from_zlo<DT>(zlb);
+                    } else {
+                        s2a = lds32(meta + (uint32_t)(ra * gmax + gl) * 4u);
+                        s2b = lds32(meta + (uint32_t)(rbw * gmax + gl) * 4u);
+                    }
+                    mac_word<DT>(acc[rb], wa.x, wb.x, zla, zha, s2a, zlb, zhb, s2b, xv[0]);
+                    mac_word<DT>(acc2[rb], wa.y, wb.y, zla, zha, s2a, zlb, zhb, s2b, xv[1]);
+                    mac_word<DT>(acc[rb], wa.z, wb.z, zla, zha, s2a, zlb, zhb, s2b, xv[2]);
+                    mac_word<DT>(acc2[rb], wa.w, wb.w, zla, zha, s2a, zlb, zhb, s2b, xv[3]);
+                }
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(empty_bar(s));
+        if (lane == 0) mbar_arrive(bar0 + 8u * (NS + s));
+        ps = s;
+        ppar = par;
+        if (++s == NS) {
+            s = 0;
+            par ^= 1u;
+        }
     }
 
-    // ---- partial sums -> shared memory: red[row block][16][8]
+    // ---- partial sums -> shared memory: red[row][m]
     float *red = reinterpret_cast<float *>(smem + L.red);
 #pragma unroll
-    for (int rb = 0; rb < R; ++rb)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[rb][e] += acc2[rb][e];
-#pragma unroll
     for (int rb = 0; rb < R; ++rb) {
-        float *r = red + ((size_t)(warp * R + rb) * 16) * 8;
-        r[g * 8 + 2 * t] = acc[rb][0];
-        r[g * 8 + 2 * t + 1] = acc[rb][1];
-        r[(g + 8) * 8 + 2 * t] = acc[rb][2];
-        r[(g + 8) * 8 + 2 * t + 1] = acc[rb][3];
+        const int r0 = (warp * R + rb) * 16;
+        red[(r0 + g) * 8 + 2 * t] = acc[rb][0] + acc2[rb][0];
+        red[(r0 + g) * 8 + 2 * t + 1] = acc[rb][1] + acc2[rb][1];
+        red[(r0 + g + 8) * 8 + 2 * t] = acc[rb][2] + acc2[rb][2];
+        red[(r0 + g + 8) * 8 + 2 * t + 1] = acc[rb][3] + acc2[rb][3];
     }
     if (S > 1) {
         cg::this_cluster().sync();
@@ -308,11 +319,11 @@ __global__ void __launch_bounds__(256) decode_kernel(const __grid_constant__ CUt
 
     // ---- reduce over the S cluster ranks; rank r writes its share of outputs
     {
-        const int total = RT * p.M;
+        const int total = RT * M;
         const int i0 = (int)((long long)rank * total / S);
         const int i1 = (int)((long long)(rank + 1) * total / S);
         for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
-            const int m = i / RT, row = i % RT;
+            const int m = i / RT, row = i - (i / RT) * RT;
             const int n = n_tile0 + row;
             if (n >= p.N) continue;
             const int off = row * 8 + m;
@@ -354,7 +365,7 @@ size_t decode_smem_bytes(const DecodeCfg &c, int M, int K, int G, bool asym) {
 bool decode_cfg_valid(const DecodeCfg &c, int M, int K, int G, bool asym) {
     if (c.R != 1 && c.R != 2) return false;
     if (c.NW != 1 && c.NW != 2 && c.NW != 4 && c.NW != 8) return false;
-    if (c.NB < 1 || c.NB > 8) return false;
+    if (c.NB != 1 && c.NB != 2 && c.NB != 4) return false;
     if (c.NS < 2 || c.NS > 8) return false;
     if (c.S < 1 || c.S > 8) return false;
     if (16 * c.R * c.NW > 256) return false;        // TMA box height limit
@@ -362,27 +373,30 @@ bool decode_cfg_valid(const DecodeCfg &c, int M, int K, int G, bool asym) {
     return true;
 }
 
+// Configuration from a measured sweep on GB300 (M = 1 decode, the
+// Qwen3-4B- and Llama-3.1-8B-shaped layers): large N wants few tall CTAs and
+// a short cluster; smaller N wants more K splits.
 DecodeCfg decode_pick_cfg(int M, int N, int K, int G, int sym, int dtype, int sm_count) {
-    (void)dtype;
-    DecodeCfg c{1, 4, 4, 4, 1};   // R, NW, NB, NS, S
+    (void)dtype; (void)sm_count;
+    DecodeCfg c;
+    if (N >= 16384)
+        c = DecodeCfg{1, 8, 2, 2, 2};
+    else if (N >= 6144)
+        c = DecodeCfg{1, 4, 4, 4, 4};
+    else
+        c = DecodeCfg{1, 4, 4, 4, 8};
     const int nblk = (K + kBoxK - 1) / kBoxK;
-    const int rt = 16 * c.R * c.NW;
-    const int tiles = (N + rt - 1) / rt;
-    // enough CTAs for ~3 per SM, split K across a cluster when rows are few
-    int S = 1;
-    while (S < 8 && tiles * S < 3 * sm_count && nblk / (S * 2) >= 2) S *= 2;
-    c.S = S;
-    const int nb = (nblk + S - 1) / S;
-    if (c.NB > nb) c.NB = nb > 0 ? nb : 1;
-    while (!decode_cfg_valid(c, M, K, G, sym == 0) && c.NS > 2) --c.NS;
+    while (c.S > 1 && nblk / c.S < 1) c.S >>= 1;            // at least one K block per CTA
+    const int nb = (nblk + c.S - 1) / c.S;
+    while (c.NB > 1 && c.NB > nb) c.NB >>= 1;                // 4, 2 or 1 boxes per stage
     while (!decode_cfg_valid(c, M, K, G, sym == 0) && c.S < 8) c.S *= 2;
     return c;
 }
 
-template <int DT, bool ASYM, int R>
+template <int DT, bool ASYM, int R, int NB>
 static cudaError_t launch_t(const CUtensorMap &tw, const DecodeParams &p, const DecodeCfg &c,
                             size_t smem, cudaStream_t s, bool pdl, int grid) {
-    auto kern = decode_kernel<DT, ASYM, R>;
+    auto kern = decode_kernel<DT, ASYM, R, NB>;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
@@ -409,6 +423,33 @@ static cudaError_t launch_t(const CUtensorMap &tw, const DecodeParams &p, const 
     cfg.attrs = attrs;
     cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, kern, tw, p);
+}
+
+template <int DT, bool ASYM>
+static cudaError_t launch_rnb(int R, int NB, const CUtensorMap &tw, const DecodeParams &p,
+                              const DecodeCfg &c, size_t smem, cudaStream_t s, bool pdl, int grid) {
+    if (R == 1) {
+        switch (NB) {
+            case 1: return launch_t<DT, ASYM, 1, 1>(tw, p, c, smem, s, pdl, grid);
+            case 2: return launch_t<DT, ASYM, 1, 2>(tw, p, c, smem, s, pdl, grid);
+            default: return launch_t<DT, ASYM, 1, 4>(tw, p, c, smem, s, pdl, grid);
+        }
+    }
+    switch (NB) {
+        case 1: return launch_t<DT, ASYM, 2, 1>(tw, p, c, smem, s, pdl, grid);
+        case 2: return launch_t<DT, ASYM, 2, 2>(tw, p, c, smem, s, pdl, grid);
+        default: return launch_t<DT, ASYM, 2, 4>(tw, p, c, smem, s, pdl, grid);
+    }
+}
+
+static cudaError_t launch_dispatch(int dtype, bool asym, int R, int NB, const CUtensorMap &tw,
+                                   const DecodeParams &p, const DecodeCfg &c, size_t smem,
+                                   cudaStream_t s, bool pdl, int grid) {
+    if (dtype == 0)
+        return asym ? launch_rnb<0, true>(R, NB, tw, p, c, smem, s, pdl, grid)
+                    : launch_rnb<0, false>(R, NB, tw, p, c, smem, s, pdl, grid);
+    return asym ? launch_rnb<1, true>(R, NB, tw, p, c, smem, s, pdl, grid)
+                : launch_rnb<1, false>(R, NB, tw, p, c, smem, s, pdl, grid);
 }
 
 cudaError_t launch_decode(const GemmArgs &a, const DecodeCfg &c, const DeviceInfo &dev,
@@ -450,16 +491,7 @@ cudaError_t launch_decode(const GemmArgs &a, const DecodeCfg &c, const DeviceInf
     const int tiles = (a.N + RT - 1) / RT;
     const int grid = tiles * c.S;
     const size_t smem = decode_smem_bytes(c, a.M, a.K, a.G, asym);
-    if (a.dtype == 0) {
-        if (asym) return c.R == 1 ? launch_t<0, true, 1>(tw, p, c, smem, s, pdl, grid)
-                                  : launch_t<0, true, 2>(tw, p, c, smem, s, pdl, grid);
-        return c.R == 1 ? launch_t<0, false, 1>(tw, p, c, smem, s, pdl, grid)
-                        : launch_t<0, false, 2>(tw, p, c, smem, s, pdl, grid);
-    }
-    if (asym) return c.R == 1 ? launch_t<1, true, 1>(tw, p, c, smem, s, pdl, grid)
-                              : launch_t<1, true, 2>(tw, p, c, smem, s, pdl, grid);
-    return c.R == 1 ? launch_t<1, false, 1>(tw, p, c, smem, s, pdl, grid)
-                    : launch_t<1, false, 2>(tw, p, c, smem, s, pdl, grid);
+    return launch_dispatch(a.dtype, asym, c.R, c.NB, tw, p, c, smem, s, pdl, grid);
 }
 
 }  // namespace w4a16

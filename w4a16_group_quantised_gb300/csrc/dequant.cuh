@@ -48,18 +48,26 @@ template <> struct Dtype<1> {
 
 __device__ __forceinline__ uint32_t rep2(uint32_t h) { return h | (h << 16); }
 
+// Packed 2 x 16-bit subtract / multiply on raw 32-bit registers, each one
+// IEEE operation rounded to nearest even (no contraction into an FMA).
 template <int DT>
 __device__ __forceinline__ uint32_t hsub2_u(uint32_t a, uint32_t b) {
-    using T2 = typename Dtype<DT>::T2;
-    T2 r = __hsub2(*reinterpret_cast<const T2 *>(&a), *reinterpret_cast<const T2 *>(&b));
-    return *reinterpret_cast<uint32_t *>(&r);
+    uint32_t r;
+    if (DT == 0)
+        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    else
+        asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
 }
 
 template <int DT>
 __device__ __forceinline__ uint32_t hmul2_u(uint32_t a, uint32_t b) {
-    using T2 = typename Dtype<DT>::T2;
-    T2 r = __hmul2_rn(*reinterpret_cast<const T2 *>(&a), *reinterpret_cast<const T2 *>(&b));
-    return *reinterpret_cast<uint32_t *>(&r);
+    uint32_t r;
+    if (DT == 0)
+        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    else
+        asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
 }
 
 // Subtrahend (M + z) for the "low" magic, in both lanes.

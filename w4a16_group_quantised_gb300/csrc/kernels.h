@@ -23,6 +23,9 @@ struct DeviceInfo {
     int max_smem_optin;
     int *status;            // device address of the status word
     void *encode_tiled;     // cuTensorMapEncodeTiled entry point
+    float *sk_ws;           // balanced decode kernel: partial sums
+    int *sk_counters;       // balanced decode kernel: per-row-block tickets (zero between calls)
+    int sk_max_rowblocks;   // capacity of sk_counters
 };
 
 // ---- pack.cu
@@ -44,6 +47,13 @@ bool decode_cfg_valid(const DecodeCfg &c, int M, int K, int G, bool asym);
 size_t decode_smem_bytes(const DecodeCfg &c, int M, int K, int G, bool asym);
 cudaError_t launch_decode(const GemmArgs &a, const DecodeCfg &c, const DeviceInfo &dev,
                           cudaStream_t s, bool pdl);
+
+// ---- decode_sk.cu (balanced skinny kernel; needs a per-device workspace)
+size_t decode_sk_smem_bytes(int M, int K);
+size_t decode_sk_workspace_floats(int sm_count);
+bool decode_sk_applicable(int M, int K);
+cudaError_t launch_decode_sk(const GemmArgs &a, int ns, const DeviceInfo &dev, float *ws, int *counters,
+                             cudaStream_t s, bool pdl);
 
 // ---- prefill.cu
 struct PrefillCfg {
