@@ -21,7 +21,9 @@
 //    canonical K-major 128-byte-swizzled layout the tensor core reads, fences
 //    them into the async proxy, and each warp arrives once on the A-ring
 //    barrier.  Scales and zero points are prefetched four steps ahead in
-//    registers.  After the main loop the same warps are the epilogue:
+//    registers, issued after that arrive (an arrive has release semantics and
+//    would otherwise wait for the prefetch to land).  After the main loop the
+//    same warps are the epilogue:
 //    tcgen05.ld from TMEM (lane quadrant = warp % 4), one rounding to the
 //    output dtype, a [BN x 256] tile staged in shared memory, one TMA store.
 //  * Warp 1: TMEM allocation (512 columns: two fp32 accumulators) and the
@@ -161,22 +163,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     grid_dependents_launch();
 
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
+        // ------------------------------------------------------------ x producer
         if (lane == 0) {
             grid_dependency_wait();  // x may be written by the previous kernel
             const uint32_t xtx = (uint32_t)p.BN * 128u;
             for (int i = 0; i < nk; ++i) {
-                if (i % kStepsPerW == 0) {
-                    const int j = i / kStepsPerW, sw = j % SW;
-                    if (!mbar_wait_bounded(wempty(sw), (uint32_t)((j / SW) & 1) ^ 1u, p.status, abort_flag))
-                        break;
-                    mbar_arrive_expect_tx(wfull(sw), (uint32_t)kWTileBytes);
-                    tma_load_2d(w_base + (uint32_t)sw * kWTileBytes, &tmap_w, wfull(sw), j * (kWK / 8), n0);
-                }
                 const int s = i % SX;
                 if (!mbar_wait_bounded(xempty(s), (uint32_t)((i / SX) & 1) ^ 1u, p.status, abort_flag)) break;
                 mbar_arrive_expect_tx(xfull(s), xtx);
                 tma_load_2d(x_base + (uint32_t)s * p.BN * 128u, &tmap_x, xfull(s), i * kBK, m0);
+            }
+        }
+    } else if (warp == 3) {
+        // ------------------------------------------------------------ weight producer
+        // (its own issuing thread: one thread's TMA boxes complete one after another)
+        if (lane == 0) {
+            const int nw = (p.K + kWK - 1) / kWK;
+            for (int j = 0; j < nw; ++j) {
+                const int sw = j % SW;
+                if (!mbar_wait_bounded(wempty(sw), (uint32_t)((j / SW) & 1) ^ 1u, p.status, abort_flag)) break;
+                mbar_arrive_expect_tx(wfull(sw), (uint32_t)kWTileBytes);
+                tma_load_2d(w_base + (uint32_t)sw * kWTileBytes, &tmap_w, wfull(sw), j * (kWK / 8), n0);
             }
         }
     } else if (warp == 1) {
@@ -245,8 +252,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         zlo = (rz_lo[d] >> zshift) & 0xFu;
                         zhi = (rz_hi[d] >> zshift) & 0xFu;
                     }
-                    load_meta(i + kScalePrefetch, rs_lo[d], rs_hi[d], rz_lo[d], rz_hi[d]);
-
                     const int j = i / kStepsPerW, jj = i % kStepsPerW, swi = j % SW;
                     if (jj == 0 &&
                         !mbar_wait_bounded(wfull(swi), (uint32_t)((j / SW) & 1), p.status, abort_flag)) {
@@ -279,6 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fence_proxy_async_smem();   // each writer: generic -> async proxy
                     __syncwarp();
                     if (lane == 0) mbar_arrive(afull(a));
+                    load_meta(i + kScalePrefetch, rs_lo[d], rs_hi[d], rz_lo[d], rz_hi[d]);
                 }
             }
         }
