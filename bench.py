@@ -13,6 +13,7 @@ measured in the same run on the Llama-3.1-8B-shaped asymmetric bf16 G = 64
 layers and reported under "prefill".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --profile-case decode|prefill --steps K --warmup W   (ncu)
 
 --impl reference times the CPU oracle (plain C, fp64) on the same workload
 (a bounded sample of steps) on the host cores.  With N > 1 (torchrun) every
@@ -75,16 +76,18 @@ def source_hash(*names):
 
 
 def profiled_traffic(kernel_tag, src_hash):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current source of that kernel (else None)."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum)
+    from the committed ncu summary profiles/traffic.txt, whose lines read
+    `<tag> <source hash> <bytes per launch>`; None unless the figure was taken
+    on the current source of that kernel."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
     try:
         with open(path) as f:
-            d = json.load(f)
-        e = d.get(kernel_tag)
-        if e and e.get("source_hash") == src_hash:
-            return e["dram_bytes_per_launch"]
-    except Exception:
+            for line in f:
+                parts = line.split()
+                if len(parts) == 3 and parts[0] == kernel_tag and parts[1] == src_hash:
+                    return int(float(parts[2]))
+    except OSError:
         pass
     return None
 
@@ -226,31 +229,47 @@ def bench_decode(w, steps, warmup, l2_bytes):
         for s in range(n_sets):   # first calls outside capture (per-device set-up)
             run_step(w, sets[s], outs)
         torch.cuda.synchronize()
+
+    def capture(n):
+        # n consecutive steps; a graph of `chunk` steps ends on the set it
+        # started from (chunk is a multiple of n_sets), so replays rotate.
         g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(chunk):
-                run_step(w, sets[i % n_sets], outs)
-    reps_w = max(1, int(np.ceil(warmup / chunk)))
-    reps = max(1, int(np.ceil(steps / chunk)))
-    with torch.cuda.stream(stream):
-        for _ in range(reps_w):
-            g.replay()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n):
+                    run_step(w, sets[i % n_sets], outs)
+        return g
+
+    graphs = {chunk: capture(chunk)}
+    for n in {steps % chunk, warmup % chunk} - {0}:
+        graphs[n] = capture(n)
+    ctx = dict(graphs=graphs, stream=stream, chunk=chunk, steps=steps, step_bytes=step_bytes,
+               n_sets=n_sets, sets=sets, outs=outs, launches_per_step=len(shapes))
+    replay_steps(ctx, warmup)
     torch.cuda.synchronize()
-    return dict(graph=g, stream=stream, chunk=chunk, reps=reps, step_bytes=step_bytes,
-                n_sets=n_sets, sets=sets, outs=outs, launches_per_step=len(shapes))
+    return ctx
+
+
+def replay_steps(ctx, n):
+    """Exactly n steps: n // chunk replays of the chunk graph, then one replay
+    of the graph of the remaining steps."""
+    chunk, graphs = ctx["chunk"], ctx["graphs"]
+    with torch.cuda.stream(ctx["stream"]):   # replay() launches on the current stream
+        for _ in range(n // chunk):
+            graphs[chunk].replay()
+        if n % chunk:
+            graphs[n % chunk].replay()
 
 
 def timed_replays(ctx, ws):
-    g, stream = ctx["graph"], ctx["stream"]
+    stream = ctx["stream"]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     barrier(ws)
     torch.cuda.synchronize()
-    with torch.cuda.stream(stream):   # replay() launches on the current stream
-        start.record(stream)
-        for _ in range(ctx["reps"]):
-            g.replay()
-        end.record(stream)
+    start.record(stream)
+    replay_steps(ctx, ctx["steps"])
+    end.record(stream)
     torch.cuda.synchronize()
     barrier(ws)
     return start.elapsed_time(end) / 1000.0
@@ -314,6 +333,28 @@ def bench_prefill(w, steps):
                                   for (ms, (_, N, K)) in zip(per_ms, shapes)])
 
 
+def profile_case(w, which, steps, warmup):
+    """A short run for ncu captures: `warmup` then `steps` eager passes over
+    the four layers of one workload (one set of inputs, launched in layer
+    order).  Prints a timing line of its own, not a bench line."""
+    if which == "decode":
+        layers = [upload(w, wl.qwen3_4b_decode(i, 1)) for i in range(len(wl.QWEN3_4B_SHAPES))]
+    else:
+        layers = [upload(w, wl.llama31_8b_prefill(i, 1920)) for i in range(len(wl.LLAMA31_8B_SHAPES))]
+    td = torch.float16 if layers[0]["dtype"] == 0 else torch.bfloat16
+    outs = [torch.empty((d["M"], d["N"]), dtype=td, device="cuda") for d in layers]
+    for _ in range(warmup):
+        run_step(w, layers, outs)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        run_step(w, layers, outs)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": which, "steps": steps, "warmup": warmup,
+                      "host_ms_per_step": (time.perf_counter() - t0) / steps * 1e3,
+                      "device_status": w.w4a16_last_device_error()}))
+
+
 def cpu_baseline(sample_steps=None, budget_s=15.0):
     """The oracle (as it stands) on the host cores, on whole decode steps."""
     import oracle
@@ -346,8 +387,11 @@ def main():
     ap.add_argument("--prefill-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--profile-case", choices=["decode", "prefill"],
+                    help="run only the short eager case that ncu captures")
     args = ap.parse_args()
     warmup = max(3, args.warmup)
+    steps = max(1, args.steps)
     ws, rank, local = dist_info()
     hbm, tc, tc_sus, peak_src = load_peaks()
 
@@ -376,9 +420,12 @@ def main():
     import w4a16_group_quantised_gb300 as w
     w.load_library()
 
+    if args.profile_case:
+        profile_case(w, args.profile_case, steps, warmup)
+        return
+
     l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size or L2_BYTES_FALLBACK
-    ctx = bench_decode(w, args.steps, warmup, l2)
-    steps = ctx["reps"] * ctx["chunk"]
+    ctx = bench_decode(w, steps, warmup, l2)
     with ClockSampler(torch.cuda.current_device()) as clk:
         dt = timed_replays(ctx, ws)
     dt = max_over_ranks(dt, ws)

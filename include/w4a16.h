@@ -161,8 +161,13 @@ int w4a16_version(void);
  * [16, 256]; the rings must fit in shared memory);
  * which = 3: programmatic dependent launch on/off, vals = {flag}, n = 1;
  * which = 4: balanced decode kernel vals = {on (1) / off (0), load ring
- * depth in units (2, 4 or 6)}, n = 2.
- * n = 0 restores the built-in choice for which = 1 or 2.  An invalid
+ * depth in units (2, 4 or 6)}, n = 2;
+ * which = 5: per-warp-stream decode kernel (for K % 128 == 0; off by
+ * default), vals = {0} off, {1} on with the built-in configuration (n = 1),
+ * or {2, NBK, S, NW, NSW} on with a forced configuration (128-k blocks per
+ * cell in {1, 2, 4}, cluster CTAs along K in 1..8, warps per CTA in {4, 8},
+ * ring slots per warp in 1..8), n = 5; n = 0 restores {0}.
+ * n = 0 restores the built-in choice for which = 1, 2, 4 or 5.  An invalid
  * configuration is rejected here or, for the decode shape limits, by the
  * next w4a16_gemm call with W4A16_ERR_ARG. */
 int w4a16_debug_set_config(int which, const int *vals, int n);

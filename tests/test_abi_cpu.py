@@ -116,6 +116,15 @@ def test_debug_config_validation(lib):
     assert lib.w4a16_debug_set_config(2, arr, 4) == 0
     assert lib.w4a16_debug_set_config(2, None, 0) == 0
     assert lib.w4a16_debug_set_config(9, None, 0) == -9
+    # per-warp-stream decode kernel: {mode} or {2, NBK, S, NW, NSW}
+    ok = (ctypes.c_int * 5)(2, 2, 4, 8, 2)
+    assert lib.w4a16_debug_set_config(5, ok, 5) == 0
+    for bad in ((2, 3, 1, 8, 2), (2, 2, 9, 8, 2), (2, 2, 1, 16, 2), (2, 2, 1, 8, 0), (3, 2, 1, 8, 2)):
+        arr = (ctypes.c_int * 5)(*bad)
+        assert lib.w4a16_debug_set_config(5, arr, 5) == -9, bad
+    assert lib.w4a16_debug_set_config(5, (ctypes.c_int * 1)(2), 1) == -9   # mode 2 needs a configuration
+    assert lib.w4a16_debug_set_config(5, (ctypes.c_int * 1)(0), 1) == 0
+    assert lib.w4a16_debug_set_config(5, None, 0) == 0
 
 
 def test_binding_rejects_wrong_zero_point_dtype():

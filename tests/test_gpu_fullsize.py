@@ -48,3 +48,19 @@ def test_llama31_8b_prefill(cuda_lib, shape, M):
     rng = np.random.default_rng(shape * 10 + M)
     rows = np.unique(np.concatenate([[0, M - 1], rng.integers(0, M, 14)])).astype(np.int32)
     _check(cuda_lib, p, rows=rows)
+
+
+@pytest.mark.parametrize("shape", [2, 3])
+def test_llama31_8b_prefill_repeatable(cuda_lib, shape):
+    """Repeated launches on the same inputs give the same bits (the prefill
+    kernel's reduction order is fixed, so any difference is a hazard)."""
+    w = cuda_lib
+    p = llama31_8b_prefill(shape, 1920)
+    d = to_device(p, w)
+    first = w.w4a16_gemm(d["x"], d["qweight"], d["scales"], d["qzeros"], p.G)
+    for _ in range(6):
+        again = w.w4a16_gemm(d["x"], d["qweight"], d["scales"], d["qzeros"], p.G)
+        torch.cuda.synchronize()
+        diff = (again.view(torch.int16) != first.view(torch.int16))
+        assert not bool(diff.any()), f"{int(diff.sum())} outputs differ between launches"
+    assert w.w4a16_last_device_error() == 0

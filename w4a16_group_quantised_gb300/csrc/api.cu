@@ -41,6 +41,10 @@ PrefillCfg g_prefill_cfg{};
 int g_pdl = 1;
 // balanced decode kernel: enabled flag and preferred ring depth
 int g_sk_on = 0, g_sk_ns = 4;
+// per-warp-stream decode kernel: 0 off (default: the cluster kernel measured faster on GB300),
+// 1 on (built-in configuration), 2 on (forced configuration)
+int g_warp_mode = 0;
+DecodeWarpCfg g_warp_cfg{2, 1, 8, 2};
 constexpr int kSkMaxRowBlocks = 1 << 16;   // N up to 1M rows
 
 void init_device(DevState &st, int dev) {
@@ -176,6 +180,23 @@ int run_gemm(const void *x, int M, int K, const int32_t *qw, const void *scales,
             decode_sk_applicable(M, K)) {
             e = launch_decode_sk(a, ns_pref, *dev, dev->sk_ws, dev->sk_counters, s, g_pdl != 0);
             return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
+        }
+        int warp_mode;
+        DecodeWarpCfg wc;
+        {
+            std::lock_guard<std::mutex> lk(g_cfg_mu);
+            warp_mode = use_cluster_override ? 0 : g_warp_mode;
+            wc = g_warp_cfg;
+        }
+        if (warp_mode != 0 && decode_warp_applicable(M, N, K)) {
+            if (warp_mode == 1)
+                wc = decode_warp_pick_cfg(M, N, K, G, qz == nullptr, dtype, dev->sm_count, dev->max_smem_optin);
+            else if (!decode_warp_cfg_valid(wc, M, N, K, G, qz != nullptr, dev->sm_count, dev->max_smem_optin))
+                return W4A16_ERR_ARG;
+            if (wc.NBK != 0) {
+                e = launch_decode_warp(a, wc, *dev, s, g_pdl != 0);
+                return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
+            }
         }
         DecodeCfg c;
         {
@@ -342,6 +363,20 @@ int w4a16_debug_set_config(int which, const int *vals, int n) {
     if (which == 3) {
         if (n != 1 || vals == nullptr) return W4A16_ERR_ARG;
         g_pdl = vals[0] != 0;
+        return W4A16_OK;
+    }
+    if (which == 5) {
+        if (n == 0) { g_warp_mode = 0; return W4A16_OK; }
+        if (vals == nullptr || (n != 1 && n != 5)) return W4A16_ERR_ARG;
+        if (vals[0] < 0 || vals[0] > 2 || (vals[0] == 2) != (n == 5)) return W4A16_ERR_ARG;
+        if (vals[0] == 2) {
+            const DecodeWarpCfg c{vals[1], vals[2], vals[3], vals[4]};
+            if (c.NBK != 1 && c.NBK != 2 && c.NBK != 4) return W4A16_ERR_ARG;
+            if (c.S < 1 || c.S > 8 || c.NSW < 1 || c.NSW > 8) return W4A16_ERR_ARG;
+            if (c.NW != 4 && c.NW != 8) return W4A16_ERR_ARG;
+            g_warp_cfg = c;
+        }
+        g_warp_mode = vals[0];
         return W4A16_OK;
     }
     if (which == 4) {

@@ -37,6 +37,7 @@
 #include "dequant.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
+#include "skinny.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -57,54 +58,6 @@ struct DecodeParams {
     int xpitch;      // bytes per x row in shared memory
     int gmax;        // max groups per CTA slice
 };
-
-template <int DT>
-__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-    if (DT == 0) {
-        asm volatile(
-            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
-            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-    } else {
-        asm volatile(
-            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
-            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-    }
-}
-
-template <int DT>
-__device__ __forceinline__ uint16_t f32_to_dt(float v) {
-    if (DT == 0) {
-        __half h = __float2half_rn(v);
-        return *reinterpret_cast<uint16_t *>(&h);
-    } else {
-        __nv_bfloat16 h = __float2bfloat16_rn(v);
-        return *reinterpret_cast<uint16_t *>(&h);
-    }
-}
-
-// Multiply one word of rows g and g+8 (4 nibble pairs each) into acc.
-template <int DT>
-__device__ __forceinline__ void mac_word(float (&acc)[4], uint32_t wa, uint32_t wb, uint32_t zla,
-                                         uint32_t zha, uint32_t s2a, uint32_t zlb, uint32_t zhb,
-                                         uint32_t s2b, uint4 xv) {
-    uint32_t oa[4], ob[4];
-    dq_word_i4<DT>(wa, zla, zha, s2a, oa);
-    dq_word_i4<DT>(wb, zlb, zhb, s2b, ob);
-    mma_16816<DT>(acc, oa[0], ob[0], oa[1], ob[1], xv.x, xv.y);
-    mma_16816<DT>(acc, oa[2], ob[2], oa[3], ob[3], xv.z, xv.w);
-}
-
-// zhi2 from zlo2: the same zero point moved from the low-magic to the
-// high-magic position in both lanes.
-template <int DT>
-__device__ __forceinline__ uint32_t zhi_from_zlo(uint32_t zl2) {
-    return ((zl2 & 0x000F000Fu) << (DT == 0 ? 4 : 3)) | rep2(Dtype<DT>::kMagicHi);
-}
 
 struct DecodeSmem {
     uint32_t ring, meta, x, red, bars, total;
@@ -133,7 +86,7 @@ __host__ __device__ inline DecodeSmem decode_layout(int R, int NW, int NB, int N
 }
 
 template <int DT, bool ASYM, int R, int NB>
-__global__ void __launch_bounds__(256) decode_kernel(const __grid_constant__ CUtensorMap tmap_w,
+__global__ void __launch_bounds__(256, R == 2 ? 3 : 1) decode_kernel(const __grid_constant__ CUtensorMap tmap_w,
                                                      const DecodeParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
@@ -228,18 +181,24 @@ __global__ void __launch_bounds__(256) decode_kernel(const __grid_constant__ CUt
     }
     __syncthreads();
 
-    // Two independent accumulator chains per row block, so consecutive MMAs
-    // do not wait on each other's results.
-    float acc[R][4], acc2[R][4];
+    // Independent accumulator chains per row block: four for one block per
+    // warp, two for two (keeps the register count, and so the CTAs per SM,
+    // of the two-block form down).
+    constexpr int NC = R == 1 ? 4 : 2;
+    float acc[R][NC][4];
 #pragma unroll
     for (int rb = 0; rb < R; ++rb)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[rb][e] = acc2[rb][e] = 0.f;
+        for (int c = 0; c < NC; ++c)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[rb][c][e] = 0.f;
 
-    const bool has_x = g < M;
-    const uint32_t xrow = sbase + L.x + (uint32_t)(g * p.xpitch) + (uint32_t)t * 16u;
-    const uint32_t meta = sbase + L.meta;
+    // Lanes whose batch column g is >= M read x row 0: their MMA output
+    // columns are never stored, so no zeroing or predication is needed.
+    const unsigned char *xrow = smem + L.x + (g < M ? g : 0) * p.xpitch + t * 16;
     const int rloc0 = warp * R * 16 + g;             // row of rb = 0 within the tile
+    constexpr int kES = ASYM ? 8 : 4;                // meta entry: {s2} or {s2, zl2}
+    const unsigned char *mrow = smem + L.meta + rloc0 * gmax * kES;
     const uint32_t zl_sym = zlo2<DT>(8u), zh_sym = zhi2<DT>(8u);
 
     bool ok = true;
@@ -254,7 +213,7 @@ __global__ void __launch_bounds__(256) decode_kernel(const __grid_constant__ CUt
             ok = false;
             break;
         }
-        const uint32_t stage = ring + (uint32_t)s * stage_bytes;
+        const unsigned char *stage = smem + L.ring + (size_t)s * stage_bytes;
         const int lb0 = step * NB;
 #pragma unroll
         for (int j = 0; j < NB; ++j) {
@@ -262,35 +221,30 @@ __global__ void __launch_bounds__(256) decode_kernel(const __grid_constant__ CUt
             if (lb < nb) {
                 const int kb = (b0 + lb) * kBoxK;
                 const int gl = min(((kb + 32 * t) >> log2G) - g0, ngs - 1);
-                uint4 xv[4];
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    xv[w] = make_uint4(0, 0, 0, 0);
-                    if (has_x) xv[w] = lds128(xrow + (uint32_t)(lb * 16 + 4 * w) * 16u);
-                }
-                const uint32_t box = stage + (uint32_t)j * RT * kBoxRowBytes + (uint32_t)t * 16u;
+                const unsigned char *xb = xrow + lb * 256;
+                const uint4 xv[4] = {sh_v4(xb), sh_v4(xb + 64), sh_v4(xb + 128), sh_v4(xb + 192)};
+                const unsigned char *box = stage + j * RT * kBoxRowBytes + t * 16 + rloc0 * kBoxRowBytes;
+                const unsigned char *mg = mrow + gl * kES;
 #pragma unroll
                 for (int rb = 0; rb < R; ++rb) {
-                    const int ra = rloc0 + rb * 16, rbw = ra + 8;
-                    const uint4 wa = lds128(box + (uint32_t)ra * kBoxRowBytes);
-                    const uint4 wb = lds128(box + (uint32_t)rbw * kBoxRowBytes);
+                    const uint4 wa = sh_v4(box + rb * 16 * kBoxRowBytes);
+                    const uint4 wb = sh_v4(box + (rb * 16 + 8) * kBoxRowBytes);
+                    const unsigned char *ma = mg + rb * 16 * gmax * kES;
                     uint32_t s2a, s2b, zla = zl_sym, zlb = zl_sym, zha = zh_sym, zhb = zh_sym;
                     if (ASYM) {
-                        const uint2 ma = lds64(meta + (uint32_t)(ra * gmax + gl) * 8u);
-                        const uint2 mb = lds64(meta + (uint32_t)(rbw * gmax + gl) * 8u);
-                        s2a = ma.x; zla = ma.y; zha = zhi_from_zlo<DT>(zla);
-                        s2b = mb.x; zlb = mb.y; zhb = zhi_from_zlo<DT>(zlb);
+                        const uint2 va = sh_v2(ma);
+                        const uint2 vb = sh_v2(ma + 8 * gmax * kES);
+                        s2a = va.x; zla = va.y; zha = zhi_from_zlo<DT>(zla);
+                        s2b = vb.x; zlb = vb.y; zhb = zhi_from_zlo<DT>(zlb);
                     } else {
-                        s2a = lds32(meta + (uint32_t)(ra * gmax + gl) * 4u);
-                        s2b = lds32(meta + (uint32_t)(rbw * gmax + gl) * 4u);
+                        s2a = sh_u32(ma);
+                        s2b = sh_u32(ma + 8 * gmax * kES);
                     }
-                    mac_word<DT>(acc[rb], wa.x, wb.x, zla, zha, s2a, zlb, zhb, s2b, xv[0]);
-                    mac_word<DT>(acc2[rb], wa.y, wb.y, zla, zha, s2a, zlb, zhb, s2b, xv[1]);
-                    mac_word<DT>(acc[rb], wa.z, wb.z, zla, zha, s2a, zlb, zhb, s2b, xv[2]);
-                    mac_word<DT>(acc2[rb], wa.w, wb.w, zla, zha, s2a, zlb, zhb, s2b, xv[3]);
+                    mac_block<DT, NC>(acc[rb], wa, wb, zla, zha, s2a, zlb, zhb, s2b, xv);
                 }
             }
         }
+        fence_proxy_async_smem();   // this warp's reads of the slot before the copy that refills it
         __syncwarp();
         if (lane == 0) mbar_arrive(bar0 + 8u * (NS + s));
         ps = s;
@@ -306,10 +260,10 @@ __global__ void __launch_bounds__(256) decode_kernel(const __grid_constant__ CUt
 #pragma unroll
     for (int rb = 0; rb < R; ++rb) {
         const int r0 = (warp * R + rb) * 16;
-        red[(r0 + g) * 8 + 2 * t] = acc[rb][0] + acc2[rb][0];
-        red[(r0 + g) * 8 + 2 * t + 1] = acc[rb][1] + acc2[rb][1];
-        red[(r0 + g + 8) * 8 + 2 * t] = acc[rb][2] + acc2[rb][2];
-        red[(r0 + g + 8) * 8 + 2 * t + 1] = acc[rb][3] + acc2[rb][3];
+        red[(r0 + g) * 8 + 2 * t] = chain_sum(acc[rb], 0);
+        red[(r0 + g) * 8 + 2 * t + 1] = chain_sum(acc[rb], 1);
+        red[(r0 + g + 8) * 8 + 2 * t] = chain_sum(acc[rb], 2);
+        red[(r0 + g + 8) * 8 + 2 * t + 1] = chain_sum(acc[rb], 3);
     }
     if (S > 1) {
         cg::this_cluster().sync();

@@ -48,6 +48,20 @@ size_t decode_smem_bytes(const DecodeCfg &c, int M, int K, int G, bool asym);
 cudaError_t launch_decode(const GemmArgs &a, const DecodeCfg &c, const DeviceInfo &dev,
                           cudaStream_t s, bool pdl);
 
+// ---- decode_warp.cu (one weight stream per warp; K a multiple of 128)
+struct DecodeWarpCfg {
+    int NBK;  // 128-k blocks per cell (1, 2, 4); a cell is 32 rows x NBK * 128 k
+    int S;    // CTAs along K in a cluster (1..8)
+    int NW;   // warps per CTA (4, 8)
+    int NSW;  // ring slots per warp (cells in flight)
+};
+bool decode_warp_applicable(int M, int N, int K);
+bool decode_warp_cfg_valid(const DecodeWarpCfg &c, int M, int N, int K, int G, bool asym, int sm_count,
+                           int smem_optin);
+DecodeWarpCfg decode_warp_pick_cfg(int M, int N, int K, int G, int sym, int dtype, int sm_count, int smem_optin);
+cudaError_t launch_decode_warp(const GemmArgs &a, const DecodeWarpCfg &c, const DeviceInfo &dev, cudaStream_t s,
+                               bool pdl);
+
 // ---- decode_sk.cu (balanced skinny kernel; needs a per-device workspace)
 size_t decode_sk_smem_bytes(int M, int K);
 size_t decode_sk_workspace_floats(int sm_count);

@@ -12,10 +12,12 @@
 //    (M = 128 per half) and the activations the shared B operand (N = BN <=
 //    256): every x tile feeds 2 x 128 x BN MACs per k, which halves the
 //    L2 -> SM activation traffic per FLOP against a 128-row tile.
-//  * Warp 0: TMA producer.  Per 64-wide K step it loads the x tile (BN rows
-//    x 128 B, 128-byte swizzle) into an SX-deep ring; every 4 steps it loads
-//    the packed weights of those 256 k (256 rows x 128 B, 128-byte swizzle)
-//    into an SW-deep ring.
+//  * Warps 0 and 3: TMA producers, one issuing thread each (a thread's TMA
+//    boxes are issued one after another, so two issuers keep more bytes in
+//    flight).  Warp 0 loads, per 64-wide K step, the x tile (BN rows x
+//    128 B, 128-byte swizzle) into an SX-deep ring; warp 3 loads the packed
+//    weights of 256 k at a time (256 rows x 128 B, 128-byte swizzle) into an
+//    SW-deep ring.
 //  * Warps 4..11: dequantisers, one weight row per thread.  Each turns its
 //    row's 32 packed bytes per step into 64 bf16/fp16 weights in the
 //    canonical K-major 128-byte-swizzled layout the tensor core reads, fences
@@ -262,6 +264,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint4 w0 = *reinterpret_cast<const uint4 *>(wrow + (((uint32_t)(2 * jj) ^ sw) << 4));
                     const uint4 w1 = *reinterpret_cast<const uint4 *>(wrow + (((uint32_t)(2 * jj + 1) ^ sw) << 4));
                     if (jj == kStepsPerW - 1 || i == nk - 1) {
+                        // Release the packed-weight slot only once this
+                        // thread's loads from it have returned (the asm
+                        // consumes the loaded registers) and are ordered
+                        // before the async-proxy copy that will refill it.
+                        asm volatile("" ::"r"(w0.x), "r"(w0.y), "r"(w0.z), "r"(w0.w), "r"(w1.x), "r"(w1.y),
+                                     "r"(w1.z), "r"(w1.w)
+                                     : "memory");
+                        fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(wempty(swi));
                     }
