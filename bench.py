@@ -14,6 +14,7 @@ layers and reported under "prefill".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
   python bench.py --profile-case decode|prefill --steps K --warmup W   (ncu)
+  python bench.py --crossover        (decode vs prefill kernel time, M = 1..16)
 
 --impl reference times the CPU oracle (plain C, fp64) on the same workload
 (a bounded sample of steps) on the host cores.  With N > 1 (torchrun) every
@@ -355,6 +356,48 @@ def profile_case(w, which, steps, warmup):
                       "device_status": w.w4a16_last_device_error()}))
 
 
+def crossover(w, reps=15):
+    """Decode vs prefill kernel time for M = 1..16 on the dispatcher sweep
+    shapes, every group size, both quantisation forms and both dtypes; L2 is
+    flushed before every launch.  Prints one JSON line per cell and a summary
+    of the largest M at which the decode kernel is still the faster one."""
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    summary = {}
+    for si, (N, K) in enumerate(wl.SWEEP_SHAPES):
+        for G in (32, 64, 128):
+            for sym in (True, False):
+                for dtype in (0, 1):
+                    td = torch.float16 if dtype == 0 else torch.bfloat16
+                    p = wl.make_problem(16, N, K, G, sym, dtype, seed=7000 + si * 100 + G + 2 * sym + dtype)
+                    d = upload(w, p)
+                    best_m = 0
+                    for M in range(1, 17):
+                        x = d["x"][:M].contiguous()
+                        out = torch.empty((M, N), dtype=td, device="cuda")
+                        times = {}
+                        for path in ((1, 2) if M <= 8 else (2,)):
+                            ts = []
+                            for r in range(reps + 2):
+                                flush.zero_()
+                                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                                e0.record()
+                                w.w4a16_gemm(x, d["qweight"], d["scales"], d["qzeros"], G, out=out, path=path)
+                                e1.record()
+                                torch.cuda.synchronize()
+                                if r >= 2:
+                                    ts.append(e0.elapsed_time(e1) * 1e3)
+                            times[path] = float(np.median(ts))
+                        if 1 in times and times[1] <= times[2]:
+                            best_m = M
+                        print(json.dumps({"crossover_cell": {"N": N, "K": K, "G": G, "sym": sym,
+                                                             "dtype": wl.DTYPE_NAME[dtype], "M": M,
+                                                             "decode_us": times.get(1), "prefill_us": times[2]}}))
+                    summary[f"{N}x{K} G{G} {'sym' if sym else 'asym'} {wl.DTYPE_NAME[dtype]}"] = best_m
+                    del d
+                    torch.cuda.empty_cache()
+    print(json.dumps({"crossover_largest_decode_m": summary}))
+
+
 def cpu_baseline(sample_steps=None, budget_s=15.0):
     """The oracle (as it stands) on the host cores, on whole decode steps."""
     import oracle
@@ -389,6 +432,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--profile-case", choices=["decode", "prefill"],
                     help="run only the short eager case that ncu captures")
+    ap.add_argument("--crossover", action="store_true",
+                    help="time both kernels at M = 1..16 (the dispatcher's threshold sweep)")
     args = ap.parse_args()
     warmup = max(3, args.warmup)
     steps = max(1, args.steps)
@@ -422,6 +467,9 @@ def main():
 
     if args.profile_case:
         profile_case(w, args.profile_case, steps, warmup)
+        return
+    if args.crossover:
+        crossover(w)
         return
 
     l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size or L2_BYTES_FALLBACK

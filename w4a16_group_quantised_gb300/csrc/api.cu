@@ -4,8 +4,9 @@
 // The dispatcher follows "[ROCm][Kernel] Add HybridW4A16LinearKernel: Triton
 // prefill + HIP skinny decode", PR description: small batch sizes (the page
 // uses M <= 5) go to the skinny split-K decode kernel, larger ones to the
-// fused-dequant GEMM.  Here the threshold is a measured table
-// (select_path_impl), bounded by the decode kernel's M <= 8.
+// fused-dequant GEMM.  Here the threshold (decode_max_m, used by
+// select_path_impl) is the measured crossover between the two kernels, which
+// on GB300 is the decode kernel's own limit, M <= 8.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -140,8 +141,14 @@ int validate_gemm(const void *x, int M, int K, const int32_t *qw, const void *sc
     return W4A16_OK;
 }
 
-// Largest M the decode kernel takes for this problem; measured crossover
-// between the two kernels (see the crossover sweep in the benchmark notes).
+// Largest M the decode kernel takes for this problem.  Measured on GB300
+// (bench.py --crossover: 2560x9728, 19456x2560 and 4096x14336, G = 32, 64,
+// 128, symmetric and asymmetric, fp16 and bf16, L2 flushed before every
+// launch): the decode kernel is the faster one at every M it supports (the
+// prefill kernel takes 1.6x to 9.7x as long at M <= 8), so the threshold is
+// the decode kernel's own limit in every cell.  The pages route M <= 5 to
+// their skinny kernel ("[ROCm][Kernel] Add HybridW4A16LinearKernel", PR
+// description).
 int decode_max_m(int N, int K, int G, int sym, int dtype) {
     (void)N; (void)K; (void)G; (void)sym; (void)dtype;
     return W4A16_MAX_DECODE_M;
