@@ -143,6 +143,24 @@ int w4a16_gemm_host(const void *x_host, int M, int K, const int32_t *qweight,
  * means qzeros_or_null == NULL. */
 int w4a16_select_path(int M, int N, int K, int G, int sym, int dtype);
 
+/* The decode GEMM (M <= 8) without any device allocation, ever.  The pages
+ * have no counterpart of this entry point: it is a library addition for
+ * callers that must not allocate device memory after start-up (an engine
+ * that reserves its whole device arena up front, or code where a cudaMalloc
+ * would synchronise the device or is not allowed).  Arguments, layouts and
+ * host-side validation are those of w4a16_gemm; the result is that of the
+ * balanced decode kernel (debug configuration which = 4).  The kernel's
+ * scratch is static device memory of fixed size, so: M must be 0..8 and N at
+ * most 131072 (W4A16_ERR_SHAPE otherwise), and the device may have at most
+ * 256 SMs (W4A16_ERR_DEVICE).  The first call on a device, with that device
+ * current, sets the scratch up (looks up its address and clears it); make
+ * that first call before any stream capture.  All calls on a device share
+ * the scratch: calls whose kernels overlap on the GPU race on it; calls in
+ * order on one stream are safe. */
+int w4a16_gemm_decode_noalloc(const void *x, int M, int K, const int32_t *qweight,
+                              const void *scales, const int32_t *qzeros_or_null, int G, int N,
+                              void *out, w4a16_stream_t stream, w4a16_dtype_t dtype);
+
 /* Device status word of the current device: W4A16_OK, or W4A16_ERR_TIMEOUT
  * if a kernel gave up a bounded wait since the last clear.  Synchronises the
  * device to read it. */

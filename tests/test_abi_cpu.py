@@ -78,6 +78,17 @@ def test_forced_path_limits(lib):
     assert ex(ALIGNED, 0, 128, ALIGNED, ALIGNED, None, 32, 64, ALIGNED, None, 0, 2) == 0
 
 
+def test_noalloc_entry_point_limits(lib):
+    """The allocation-free decode entry point validates on the host like
+    w4a16_gemm and rejects what its static scratch cannot hold."""
+    f = lib.w4a16_gemm_decode_noalloc
+    assert f(ALIGNED, 9, 128, ALIGNED, ALIGNED, None, 32, 64, ALIGNED, None, 0) == -2     # M > 8
+    assert f(ALIGNED, 1, 128, ALIGNED, ALIGNED, None, 32, 131080, ALIGNED, None, 0) == -2  # N > 131072
+    assert f(ALIGNED, 1, 128, ALIGNED, ALIGNED, None, 48, 64, ALIGNED, None, 0) == -3     # group size
+    assert f(MISALIGNED, 1, 128, ALIGNED, ALIGNED, None, 32, 64, ALIGNED, None, 0) == -4
+    assert f(None, 0, 128, ALIGNED, ALIGNED, None, 32, 64, None, None, 0) == 0            # M == 0
+
+
 def test_pack_validation(lib):
     assert lib.w4a16_pack(ALIGNED, 8, 12, ALIGNED, None) == -2     # K % 8
     assert lib.w4a16_pack(NULL, 8, 16, ALIGNED, None) == -1

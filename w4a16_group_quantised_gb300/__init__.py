@@ -17,6 +17,7 @@ from .binding import (  # noqa: F401
     w4a16_debug_set_config,
     w4a16_dequant_debug,
     w4a16_gemm,
+    w4a16_gemm_decode_noalloc,
     w4a16_gemm_host,
     w4a16_last_device_error,
     w4a16_pack,

@@ -57,6 +57,7 @@ def load_library():
             "w4a16_gemm_bf16": [P, I, I, P, P, P, I, I, P, P],
             "w4a16_gemm_ex": [P, I, I, P, P, P, I, I, P, P, I, I],
             "w4a16_gemm_host": [P, I, I, P, P, P, I, I, P, I, P, P, P],
+            "w4a16_gemm_decode_noalloc": [P, I, I, P, P, P, I, I, P, P, I],
             "w4a16_select_path": [I, I, I, I, I, I],
             "w4a16_last_device_error": [],
             "w4a16_clear_device_error": [],
@@ -176,6 +177,25 @@ def w4a16_gemm_host(x_host, qweight, scales, qzeros, G: int, out_host, dev_x, de
                              _p(out_host), dt, _p(dev_x), _p(dev_out), _stream_ptr(stream))
     _check("w4a16_gemm_host", rc)
     return out_host
+
+
+def w4a16_gemm_decode_noalloc(x, qweight, scales, qzeros, G: int, out=None, stream=None):
+    """y = x . dequant(W)^T for M <= 8 through the allocation-free entry point
+    (static device scratch; see include/w4a16.h).  `out` must be given by a
+    caller that must not allocate; if it is None a tensor is created here."""
+    import torch
+    lib = load_library()
+    _require_int32("qzeros", qzeros)
+    _require_int32("qweight", qweight)
+    M, K = x.shape
+    N = qweight.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=x.dtype, device=x.device)
+    rc = lib.w4a16_gemm_decode_noalloc(_p(x), M, K, _p(qweight), _p(scales),
+                                       _p(qzeros) if qzeros is not None else None, G, N, _p(out),
+                                       _stream_ptr(stream), _dtype_code(x))
+    _check("w4a16_gemm_decode_noalloc", rc)
+    return out
 
 
 def w4a16_select_path(M: int, N: int, K: int, G: int, sym: bool, dtype: int) -> int:

@@ -226,6 +226,21 @@ int run_gemm(const void *x, int M, int K, const int32_t *qw, const void *scales,
 }
 
 }  // namespace
+
+// Shared with the allocation-free entry point (noalloc.cu): the same host
+// validation, and the status word's device address (no device state is
+// created here).
+int validate_gemm_args(const void *x, int M, int K, const int32_t *qw, const void *scales, const int32_t *qz,
+                       int G, int N, const void *out, int dtype) {
+    return validate_gemm(x, M, K, qw, scales, qz, G, N, out, dtype);
+}
+
+int *device_status_word() {
+    void *sym = nullptr;
+    if (cudaGetSymbolAddress(&sym, g_w4a16_status) != cudaSuccess) return nullptr;
+    return static_cast<int *>(sym);
+}
+
 }  // namespace w4a16
 
 using namespace w4a16;

@@ -69,6 +69,11 @@ bool decode_sk_applicable(int M, int K);
 cudaError_t launch_decode_sk(const GemmArgs &a, int ns, const DeviceInfo &dev, float *ws, int *counters,
                              cudaStream_t s, bool pdl);
 
+// ---- api.cu helpers used by noalloc.cu
+int validate_gemm_args(const void *x, int M, int K, const int32_t *qw, const void *scales, const int32_t *qz,
+                       int G, int N, const void *out, int dtype);
+int *device_status_word();
+
 // ---- prefill.cu
 struct PrefillCfg {
     int BN;       // tokens per tile (MMA N), multiple of 16, <= 256
