@@ -22,10 +22,10 @@
 //    row's 32 packed bytes per step into 64 bf16/fp16 weights in the
 //    canonical K-major 128-byte-swizzled layout the tensor core reads, fences
 //    them into the async proxy, and each warp arrives once on the A-ring
-//    barrier.  Scales and zero points are prefetched four steps ahead in
-//    registers, issued after that arrive (an arrive has release semantics and
-//    would otherwise wait for the prefetch to land).  After the main loop the
-//    same warps are the epilogue:
+//    barrier.  Scales and zero points come one packed-weight tile ahead, one
+//    vector load per tile, issued after the tile's first arrive (an arrive
+//    has release semantics and would otherwise wait for the loads to land).
+//    After the main loop the same warps are the epilogue:
 //    tcgen05.ld from TMEM (lane quadrant = warp % 4), one rounding to the
 //    output dtype, a [BN x 256] tile staged in shared memory, one TMA store.
 //  * Warp 1: TMEM allocation (512 columns: two fp32 accumulators) and the
@@ -52,7 +52,6 @@ constexpr int kThreads = 384;                  // 12 warps
 constexpr int kDeqWarps = 8;
 constexpr int kATileBytes = kBW * kBK * 2;     // 32 KB: both halves
 constexpr int kWTileBytes = kBW * kWK / 2;     // 32 KB packed
-constexpr int kScalePrefetch = 4;
 
 struct PrefillParams {
     const uint16_t *scales;
@@ -218,23 +217,79 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = n0 + r;
         const bool vrow = n < p.N;
         const int zshift = 4 * (n & 7);
-        uint32_t rs_lo[kScalePrefetch], rs_hi[kScalePrefetch], rz_lo[kScalePrefetch], rz_hi[kScalePrefetch];
-        auto load_meta = [&](int i, uint32_t &slo, uint32_t &shi, uint32_t &zlo, uint32_t &zhi) {
-            slo = shi = 0u;
-            zlo = zhi = 0u;
-            if (i < nk && vrow) {
-                const int k_lo = i * kBK, k_hi = i * kBK + 32;
-                const int g_lo = k_lo / p.G, g_hi = k_hi / p.G;
-                slo = __ldg(p.scales + (size_t)n * p.ng + g_lo);
-                if (ASYM) zlo = (uint32_t)__ldg(p.qz + (size_t)(n >> 3) * p.ng + g_lo);
-                if (k_hi < p.K) {
-                    shi = __ldg(p.scales + (size_t)n * p.ng + g_hi);
-                    if (ASYM) zhi = (uint32_t)__ldg(p.qz + (size_t)(n >> 3) * p.ng + g_hi);
+        // Scales and zero points: the groups of one packed-weight tile (256 k)
+        // for this row are fetched with one vector load each (K a multiple
+        // of 256 keeps them aligned; else one load per group), one tile
+        // ahead, right after the tile's first A-ring arrive -- so that the
+        // loads neither sit behind the dequantiser's shared-memory stores
+        // every step nor hold up a release-arrive while they are in flight.
+        // At the start of a tile they are unpacked into per-step registers.
+        const int gcount = kWK / p.G;                  // groups per tile: 8, 4 or 2
+        const bool vec_meta = (p.K % kWK) == 0;
+        uint32_t vs[4], vz[8];
+        auto load_tile_meta = [&](int j) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) vs[e] = 0u;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) vz[e] = 0u;
+            if (!vrow || j * kWK >= p.K) return;
+            const int gA = j * gcount;
+            const uint16_t *sp = p.scales + (size_t)n * p.ng + gA;
+            const int32_t *zp = ASYM ? p.qz + (size_t)(n >> 3) * p.ng + gA : nullptr;
+            if (vec_meta) {
+                if (gcount == 8) {
+                    const uint4 v = ldg_nc_v4(sp);
+                    vs[0] = v.x; vs[1] = v.y; vs[2] = v.z; vs[3] = v.w;
+                    if (ASYM) {
+                        const uint4 z0 = ldg_nc_v4(zp), z1 = ldg_nc_v4(zp + 4);
+                        vz[0] = z0.x; vz[1] = z0.y; vz[2] = z0.z; vz[3] = z0.w;
+                        vz[4] = z1.x; vz[5] = z1.y; vz[6] = z1.z; vz[7] = z1.w;
+                    }
+                } else if (gcount == 4) {
+                    const uint2 v = ldg_nc_v2(sp);
+                    vs[0] = v.x; vs[1] = v.y;
+                    if (ASYM) {
+                        const uint4 z0 = ldg_nc_v4(zp);
+                        vz[0] = z0.x; vz[1] = z0.y; vz[2] = z0.z; vz[3] = z0.w;
+                    }
+                } else {
+                    vs[0] = ldg_nc_u32(sp);
+                    if (ASYM) {
+                        const uint2 z0 = ldg_nc_v2(zp);
+                        vz[0] = z0.x; vz[1] = z0.y;
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    if (g < gcount && gA + g < p.ng) {
+                        const uint32_t h = __ldg(sp + g);
+                        vs[g >> 1] |= (g & 1) ? (h << 16) : h;
+                        if (ASYM) vz[g] = (uint32_t)__ldg(zp + g);
+                    }
                 }
             }
         };
+        // per-step (k and k + 32 halves of each 64-wide step) scale and zero word
+        uint32_t rs_lo[kStepsPerW], rs_hi[kStepsPerW], rz_lo[kStepsPerW], rz_hi[kStepsPerW];
+        auto unpack_tile_meta = [&]() {
 #pragma unroll
-        for (int d = 0; d < kScalePrefetch; ++d) load_meta(d, rs_lo[d], rs_hi[d], rz_lo[d], rz_hi[d]);
+            for (int jj = 0; jj < kStepsPerW; ++jj) {
+                if (gcount == 8) {          // G = 32: groups 2jj, 2jj + 1
+                    rs_lo[jj] = vs[jj] & 0xFFFFu;
+                    rs_hi[jj] = vs[jj] >> 16;
+                    rz_lo[jj] = vz[2 * jj];
+                    rz_hi[jj] = vz[2 * jj + 1];
+                } else if (gcount == 4) {   // G = 64: group jj
+                    rs_lo[jj] = rs_hi[jj] = (jj & 1) ? (vs[jj >> 1] >> 16) : (vs[jj >> 1] & 0xFFFFu);
+                    rz_lo[jj] = rz_hi[jj] = vz[jj];
+                } else {                    // G = 128: group jj / 2
+                    rs_lo[jj] = rs_hi[jj] = (jj >> 1) ? (vs[0] >> 16) : (vs[0] & 0xFFFFu);
+                    rz_lo[jj] = rz_hi[jj] = vz[jj >> 1];
+                }
+            }
+        };
+        load_tile_meta(0);
 
         // A tile (both halves): half h = r / 128 at h * 16 KB; 128-byte rows,
         // 16-byte chunk c of row r at position c ^ (r % 8) within its 8-row atom.
@@ -243,9 +298,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                sw * 128u;
         const uint32_t w_row = (uint32_t)(r >> 3) * 1024u + sw * 128u;   // packed tile, same swizzle
         bool ok = true;
-        for (int i0 = 0; i0 < nk && ok; i0 += kScalePrefetch) {
+        for (int i0 = 0; i0 < nk && ok; i0 += kStepsPerW) {
+            unpack_tile_meta();
 #pragma unroll
-            for (int d = 0; d < kScalePrefetch; ++d) {
+            for (int d = 0; d < kStepsPerW; ++d) {
                 const int i = i0 + d;
                 if (i < nk && ok) {
                     const uint32_t slo = rs_lo[d], shi = rs_hi[d];
@@ -294,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fence_proxy_async_smem();   // each writer: generic -> async proxy
                     __syncwarp();
                     if (lane == 0) mbar_arrive(afull(a));
-                    load_meta(i + kScalePrefetch, rs_lo[d], rs_hi[d], rz_lo[d], rz_hi[d]);
+                    if (d == 0) load_tile_meta(i / kStepsPerW + 1);
                 }
             }
         }
