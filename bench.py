@@ -498,7 +498,7 @@ def main():
     dom = int(np.argmax(pre["per_shape_ms"]))
     tc_peak = tc_sus if tc_sus else tc
 
-    dec_hash = source_hash("decode.cu", "dequant.cuh", "ptx.cuh")
+    dec_hash = source_hash("decode.cu", "skinny.cuh", "dequant.cuh", "ptx.cuh")
     pre_hash = source_hash("prefill.cu", "dequant.cuh", "ptx.cuh")
     status = w.w4a16_last_device_error()
 
