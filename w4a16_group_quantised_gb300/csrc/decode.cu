@@ -140,22 +140,43 @@ __global__ void __launch_bounds__(256, R == 2 ? 3 : 1) decode_kernel(const __gri
         for (int st = 0; st < min(NS, nsteps); ++st) issue(st);
     }
 
-    // ---- per-(row, group) constants of the slice (static: before the dependency wait)
-    for (int i = threadIdx.x; i < RT * ngs; i += blockDim.x) {
-        const int r = i / ngs, gg = i - (i / ngs) * ngs;
+    // ---- per-(row, group) constants of the slice (static: before the dependency wait).
+    // RT is a power of two and the CTA has 2 / R threads per row; each thread
+    // walks its row's groups with that stride, four loads in flight at a time.
+    constexpr int kES = ASYM ? 8 : 4;                // meta entry: {s2} or {s2, zl2}
+    {
+        const int tpr = (int)blockDim.x / RT;
+        const int r = (int)threadIdx.x & (RT - 1), gs = (int)threadIdx.x / RT;
         const int n = n_tile0 + r;
-        uint32_t s2 = 0u, zl2 = zlo2<DT>(8u);
-        if (n < p.N) {
-            s2 = rep2(__ldg(p.scales + (size_t)n * p.ng + g0 + gg));
-            if (ASYM) {
-                const uint32_t zw = (uint32_t)__ldg(p.qz + (size_t)(n >> 3) * p.ng + g0 + gg);
-                zl2 = zlo2<DT>((zw >> (4 * (n & 7))) & 0xFu);
+        const bool vr = n < p.N;
+        const uint16_t *srow = p.scales + (size_t)(vr ? n : 0) * p.ng + g0;
+        const int32_t *zrow = ASYM ? p.qz + (size_t)((vr ? n : 0) >> 3) * p.ng + g0 : nullptr;
+        const int zsh = 4 * (n & 7);
+        unsigned char *mw = smem + L.meta + (size_t)r * gmax * kES;
+        for (int gg0 = gs; gg0 < ngs; gg0 += 4 * tpr) {
+            uint32_t sv[4], zv[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int gg = gg0 + j * tpr;
+                sv[j] = 0u;
+                zv[j] = 0x88888888u;
+                if (vr && gg < ngs) {
+                    sv[j] = __ldg(srow + gg);
+                    if (ASYM) zv[j] = (uint32_t)__ldg(zrow + gg);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int gg = gg0 + j * tpr;
+                if (gg < ngs) {
+                    if (ASYM)
+                        *reinterpret_cast<uint2 *>(mw + gg * 8) =
+                            make_uint2(rep2(sv[j]), zlo2<DT>((zv[j] >> zsh) & 0xFu));
+                    else
+                        *reinterpret_cast<uint32_t *>(mw + gg * 4) = rep2(sv[j]);
+                }
             }
         }
-        if (ASYM)
-            *reinterpret_cast<uint2 *>(smem + L.meta + ((size_t)r * gmax + gg) * 8) = make_uint2(s2, zl2);
-        else
-            *reinterpret_cast<uint32_t *>(smem + L.meta + ((size_t)r * gmax + gg) * 4) = s2;
     }
 
     // ---- x slice -> shared memory, permuted; zero for k >= K
@@ -197,7 +218,6 @@ __global__ void __launch_bounds__(256, R == 2 ? 3 : 1) decode_kernel(const __gri
     // columns are never stored, so no zeroing or predication is needed.
     const unsigned char *xrow = smem + L.x + (g < M ? g : 0) * p.xpitch + t * 16;
     const int rloc0 = warp * R * 16 + g;             // row of rb = 0 within the tile
-    constexpr int kES = ASYM ? 8 : 4;                // meta entry: {s2} or {s2, zl2}
     const unsigned char *mrow = smem + L.meta + rloc0 * gmax * kES;
     const uint32_t zl_sym = zlo2<DT>(8u), zh_sym = zhi2<DT>(8u);
 
