@@ -52,6 +52,7 @@ struct DecodeParams {
     const int32_t *qz;
     uint16_t *out;
     int *status;
+    DqConsts dq;          // dequantiser masks / magics, passed as data (see dequant.cuh)
     int M, N, K, G, ng, log2G;
     int NW, NB, NS, S;
     int nblk;        // K blocks of 128 (the last one may be partial)
@@ -220,6 +221,7 @@ __global__ void __launch_bounds__(256, R == 2 ? 3 : 1) decode_kernel(const __gri
     const int rloc0 = warp * R * 16 + g;             // row of rb = 0 within the tile
     const unsigned char *mrow = smem + L.meta + rloc0 * gmax * kES;
     const uint32_t zl_sym = zlo2<DT>(8u), zh_sym = zhi2<DT>(8u);
+    const DqConsts dc = p.dq;
 
     bool ok = true;
     int s = 0, ps = NS - 1;                  // ring slot of this step and of the previous one
@@ -260,7 +262,7 @@ __global__ void __launch_bounds__(256, R == 2 ? 3 : 1) decode_kernel(const __gri
                         s2a = sh_u32(ma);
                         s2b = sh_u32(ma + 8 * gmax * kES);
                     }
-                    mac_block<DT, NC>(acc[rb], wa, wb, zla, zha, s2a, zlb, zhb, s2b, xv);
+                    mac_block<DT, NC>(acc[rb], dc, wa, wb, zla, zha, s2a, zlb, zhb, s2b, xv);
                 }
             }
         }
@@ -449,6 +451,7 @@ cudaError_t launch_decode(const GemmArgs &a, const DecodeCfg &c, const DeviceInf
     p.qz = a.qzeros;
     p.out = (uint16_t *)a.out;
     p.status = dev.status;
+    p.dq = dq_consts_i4(a.dtype);
     p.M = a.M;
     p.N = a.N;
     p.K = a.K;

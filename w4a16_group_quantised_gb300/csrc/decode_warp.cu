@@ -56,6 +56,7 @@ struct WParams {
     const int32_t *qz;
     uint16_t *out;
     int *status;
+    DqConsts dq;          // dequantiser masks / magics, passed as data (see dequant.cuh)
     int M, N, K, ng, log2G;
     int U, T, S, C, KB;          // row units, row groups, K splits, K columns, 128-k blocks
     int NW, NSW;
@@ -192,6 +193,7 @@ __global__ void __launch_bounds__(256, 2) decode_warp_kernel(const __grid_consta
     // columns are never stored.
     const unsigned char *xrow = smem + p.off_x + (g < M ? g : 0) * p.xpitch + t * 16;
     const uint32_t zl_sym = zlo2<DT>(8u), zh_sym = zhi2<DT>(8u);
+    const DqConsts dc = p.dq;
     const int log2G = p.log2G;
 
     // Partial sums of a finished row unit -> red[warp][seg][row][m] (m < M).
@@ -248,7 +250,7 @@ __global__ void __launch_bounds__(256, 2) decode_warp_kernel(const __grid_consta
                         s2a = sh_u32(ma);
                         s2b = sh_u32(ma + mstep);
                     }
-                    mac_block<DT, 4>(acc[rb], wa, wb, zla, zha, s2a, zlb, zhb, s2b, xv);
+                    mac_block<DT, 4>(acc[rb], dc, wa, wb, zla, zha, s2a, zlb, zhb, s2b, xv);
                 }
             }
         }
@@ -486,6 +488,7 @@ cudaError_t launch_decode_warp(const GemmArgs &a, const DecodeWarpCfg &c, const 
     p.qz = a.qzeros;
     p.out = (uint16_t *)a.out;
     p.status = dev.status;
+    p.dq = dq_consts_i4(a.dtype);
     p.M = a.M;
     p.N = a.N;
     p.K = a.K;

@@ -81,6 +81,68 @@ __device__ __forceinline__ uint32_t zhi2(uint32_t z) {
     return rep2(Dtype<DT>::kMagicHi | (DT == 0 ? (z << 4) : (z << 3)));
 }
 
+// The masks and magic words of the two pairings, held in registers.  The
+// kernels take them from their launch parameters, so the compiler cannot
+// turn them back into immediates: a three-input logic operation accepts at
+// most one immediate, and (x & mask) | magic with two immediates costs two
+// instructions instead of one.
+struct DqConsts {
+    uint32_t m0, m1;   // nibble masks
+    uint32_t g0, g1;   // magic words (both lanes)
+};
+
+// (k, k+4) pairing (dq_word_i4_rt): fp16 nibbles at bits 0..3 / 4..7 of each
+// lane; bf16 nibbles at bits 0..3 / 3..6.
+__host__ __device__ inline DqConsts dq_consts_i4(int dtype) {
+    if (dtype == 0) return DqConsts{0x000F000Fu, 0x00F000F0u, 0x64006400u, 0x54005400u};
+    return DqConsts{0x000F000Fu, 0x00780078u, 0x43004300u, 0x41804180u};
+}
+// natural pairing (dq_word_seq_rt): fp16 low lane bits 0..3 (magic 1024),
+// high lane bits 4..7 (magic 64); bf16 both lanes bits 0..3 (magic 128).
+__host__ __device__ inline DqConsts dq_consts_seq(int dtype) {
+    if (dtype == 0) return DqConsts{0x00F0000Fu, 0u, 0x54006400u, 0u};
+    return DqConsts{0x000F000Fu, 0u, 0x43004300u, 0u};
+}
+
+template <int DT>
+__device__ __forceinline__ void dq_word_i4_rt(uint32_t w, const DqConsts &c, uint32_t zl2, uint32_t zh2,
+                                              uint32_t s2, uint32_t (&o)[4]) {
+    uint32_t v0, v1, v2, v3;
+    const uint32_t w8 = w >> 8;
+    v0 = (w & c.m0) | c.g0;
+    v2 = (w8 & c.m0) | c.g0;
+    if (DT == 0) {
+        v1 = (w & c.m1) | c.g1;
+        v3 = (w8 & c.m1) | c.g1;
+    } else {
+        v1 = ((w >> 1) & c.m1) | c.g1;
+        v3 = ((w >> 9) & c.m1) | c.g1;
+    }
+    o[0] = hmul2_u<DT>(hsub2_u<DT>(v0, zl2), s2);
+    o[1] = hmul2_u<DT>(hsub2_u<DT>(v1, zh2), s2);
+    o[2] = hmul2_u<DT>(hsub2_u<DT>(v2, zl2), s2);
+    o[3] = hmul2_u<DT>(hsub2_u<DT>(v3, zh2), s2);
+}
+
+template <int DT>
+__device__ __forceinline__ void dq_word_seq_rt(uint32_t w, const DqConsts &c, uint32_t zc2, uint32_t s2,
+                                               uint32_t (&o)[4]) {
+    if (DT == 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t b = __byte_perm(w, 0u, (uint32_t)(i | (i << 8)));
+            o[i] = hmul2_u<0>(hsub2_u<0>((b & c.m0) | c.g0, zc2), s2);
+        }
+    } else {
+        const uint32_t t = w >> 4;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t b = __byte_perm(w, t, (uint32_t)(i | ((4 + i) << 8)));
+            o[i] = hmul2_u<1>(hsub2_u<1>((b & c.m0) | c.g0, zc2), s2);
+        }
+    }
+}
+
 // Natural-order pairs.  o[i] = (w_{2i}, w_{2i+1}) for nibbles 2i, 2i+1 of word.
 // zc2 = (M_lo + z, M_hi + z) for fp16, (M_lo + z, M_lo + z) for bf16; s2 = (s, s).
 template <int DT>

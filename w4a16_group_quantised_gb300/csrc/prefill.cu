@@ -54,6 +54,7 @@ constexpr int kATileBytes = kBW * kBK * 2;     // 32 KB: both halves
 constexpr int kWTileBytes = kBW * kWK / 2;     // 32 KB packed
 
 struct PrefillParams {
+    DqConsts dq;          // dequantiser masks / magics, passed as data (see dequant.cuh)
     const uint16_t *scales;
     const int32_t *qz;
     int M, N, K, G, ng;
@@ -297,6 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a_row = (uint32_t)(r >> 7) * (kHalf * 128) + (uint32_t)((r & 127) >> 3) * 1024u +
                                sw * 128u;
         const uint32_t w_row = (uint32_t)(r >> 3) * 1024u + sw * 128u;   // packed tile, same swizzle
+        const DqConsts dc = p.dq;
         bool ok = true;
         for (int i0 = 0; i0 < nk && ok; i0 += kStepsPerW) {
             unpack_tile_meta();
@@ -343,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
                         uint32_t o[4];
-                        dq_word_seq<DT>(words[c], c < 4 ? zc_lo : zc_hi, c < 4 ? s2lo : s2hi, o);
+                        dq_word_seq_rt<DT>(words[c], dc, c < 4 ? zc_lo : zc_hi, c < 4 ? s2lo : s2hi, o);
                         *reinterpret_cast<uint4 *>(adst + (((uint32_t)c ^ sw) << 4)) =
                             make_uint4(o[0], o[1], o[2], o[3]);
                     }
@@ -502,6 +504,7 @@ cudaError_t launch_prefill(const GemmArgs &a, const PrefillCfg &c, const DeviceI
             return cudaErrorInvalidValue;
     }
     PrefillParams p;
+    p.dq = dq_consts_seq(a.dtype);
     p.scales = (const uint16_t *)a.scales;
     p.qz = a.qzeros;
     p.M = a.M;

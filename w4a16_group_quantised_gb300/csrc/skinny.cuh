@@ -34,12 +34,12 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 // xv = the matching x pairs: (x_k, x_k+4), (x_k+1, x_k+5), (x_k+2, x_k+6),
 // (x_k+3, x_k+7) of batch column g.
 template <int DT>
-__device__ __forceinline__ void mac_word(float (&c0)[4], float (&c1)[4], uint32_t wa, uint32_t wb, uint32_t zla,
-                                         uint32_t zha, uint32_t s2a, uint32_t zlb, uint32_t zhb, uint32_t s2b,
-                                         uint4 xv) {
+__device__ __forceinline__ void mac_word(float (&c0)[4], float (&c1)[4], const DqConsts &dc, uint32_t wa, uint32_t wb,
+                                         uint32_t zla, uint32_t zha, uint32_t s2a, uint32_t zlb, uint32_t zhb,
+                                         uint32_t s2b, uint4 xv) {
     uint32_t oa[4], ob[4];
-    dq_word_i4<DT>(wa, zla, zha, s2a, oa);
-    dq_word_i4<DT>(wb, zlb, zhb, s2b, ob);
+    dq_word_i4_rt<DT>(wa, dc, zla, zha, s2a, oa);
+    dq_word_i4_rt<DT>(wb, dc, zlb, zhb, s2b, ob);
     mma16816<DT>(c0, oa[0], ob[0], oa[1], ob[1], xv.x, xv.y);
     mma16816<DT>(c1, oa[2], ob[2], oa[3], ob[3], xv.z, xv.w);
 }
@@ -48,14 +48,14 @@ __device__ __forceinline__ void mac_word(float (&c0)[4], float (&c1)[4], uint32_
 // chains (words alternate between the pairs (0, 1) and (2, 3)) or NC = 2
 // chains (every word into (0, 1)).
 template <int DT, int NC>
-__device__ __forceinline__ void mac_block(float (&acc)[NC][4], uint4 wa, uint4 wb, uint32_t zla, uint32_t zha,
-                                          uint32_t s2a, uint32_t zlb, uint32_t zhb, uint32_t s2b,
+__device__ __forceinline__ void mac_block(float (&acc)[NC][4], const DqConsts &dc, uint4 wa, uint4 wb, uint32_t zla,
+                                          uint32_t zha, uint32_t s2a, uint32_t zlb, uint32_t zhb, uint32_t s2b,
                                           const uint4 (&xv)[4]) {
     constexpr int P = NC == 4 ? 2 : 0;
-    mac_word<DT>(acc[0], acc[1], wa.x, wb.x, zla, zha, s2a, zlb, zhb, s2b, xv[0]);
-    mac_word<DT>(acc[P], acc[P + 1], wa.y, wb.y, zla, zha, s2a, zlb, zhb, s2b, xv[1]);
-    mac_word<DT>(acc[0], acc[1], wa.z, wb.z, zla, zha, s2a, zlb, zhb, s2b, xv[2]);
-    mac_word<DT>(acc[P], acc[P + 1], wa.w, wb.w, zla, zha, s2a, zlb, zhb, s2b, xv[3]);
+    mac_word<DT>(acc[0], acc[1], dc, wa.x, wb.x, zla, zha, s2a, zlb, zhb, s2b, xv[0]);
+    mac_word<DT>(acc[P], acc[P + 1], dc, wa.y, wb.y, zla, zha, s2a, zlb, zhb, s2b, xv[1]);
+    mac_word<DT>(acc[0], acc[1], dc, wa.z, wb.z, zla, zha, s2a, zlb, zhb, s2b, xv[2]);
+    mac_word<DT>(acc[P], acc[P + 1], dc, wa.w, wb.w, zla, zha, s2a, zlb, zhb, s2b, xv[3]);
 }
 
 // Sum of the chains, element e, in a fixed order.
