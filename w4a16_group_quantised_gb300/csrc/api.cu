@@ -62,6 +62,7 @@ void init_device(DevState &st, int dev) {
         return;
     }
     if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
             cudaSuccess) {
         st.rc = W4A16_ERR_CUDA;
@@ -209,7 +210,7 @@ int run_gemm(const void *x, int M, int K, const int32_t *qw, const void *scales,
         {
             std::lock_guard<std::mutex> lk(g_cfg_mu);
             c = g_decode_override ? g_decode_cfg
-                                  : decode_pick_cfg(M, N, K, G, qz == nullptr, dtype, dev->sm_count);
+                                  : decode_pick_cfg(M, N, K, G, qz == nullptr, dtype, dev->sm_count, dev->smem_per_sm);
         }
         if (!decode_cfg_valid(c, M, K, G, qz != nullptr)) return W4A16_ERR_ARG;
         e = launch_decode(a, c, *dev, s, g_pdl != 0);

@@ -31,6 +31,7 @@
 //    early launch.
 //  * Every mbarrier wait is bounded; on a timeout the status word is set and
 //    the CTA leaves its loop.
+#include <algorithm>
 #include <cooperative_groups.h>
 #include <cuda.h>
 
@@ -349,13 +350,20 @@ bool decode_cfg_valid(const DecodeCfg &c, int M, int K, int G, bool asym) {
     return true;
 }
 
-// Configuration from a measured sweep on GB300 (M = 1 decode, the
-// Qwen3-4B- and Llama-3.1-8B-shaped layers): large N wants few tall CTAs and
-// a short cluster; smaller N wants more K splits.
-DecodeCfg decode_pick_cfg(int M, int N, int K, int G, int sym, int dtype, int sm_count) {
-    (void)dtype; (void)sm_count;
+// Configuration from measured sweeps on GB300 (M = 1 decode, the Qwen3-4B-
+// and Llama-3.1-8B-shaped layers, CUDA graphs with programmatic dependent
+// launch, both per layer and over the four layers of a step in sequence,
+// where a layer's CTAs must leave room for the next layer's to start early):
+// one 16-row block per warp, 128-k boxes, K split into more cluster CTAs as N
+// shrinks.  The ring is then made as deep as it can be while the whole grid
+// stays resident on the SMs at once (a deeper ring that pushes CTAs into a
+// second wave measured slower than a shallow one).
+DecodeCfg decode_pick_cfg(int M, int N, int K, int G, int sym, int dtype, int sm_count, int smem_per_sm) {
+    (void)dtype;
     DecodeCfg c;
-    if (N >= 16384)
+    if (N >= 24576)
+        c = DecodeCfg{1, 4, 4, 2, 1};
+    else if (N >= 16384)
         c = DecodeCfg{1, 8, 2, 2, 2};
     else if (N >= 6144)
         c = DecodeCfg{1, 4, 4, 4, 4};
@@ -366,6 +374,15 @@ DecodeCfg decode_pick_cfg(int M, int N, int K, int G, int sym, int dtype, int sm
     const int nb = (nblk + c.S - 1) / c.S;
     while (c.NB > 1 && c.NB > nb) c.NB >>= 1;                // 4, 2 or 1 boxes per stage
     while (!decode_cfg_valid(c, M, K, G, sym == 0) && c.S < 8) c.S *= 2;
+    const int RT = 16 * c.R * c.NW;
+    const long long grid = (long long)((N + RT - 1) / RT) * c.S;
+    for (; c.NS > 2; --c.NS) {
+        if (!decode_cfg_valid(c, M, K, G, sym == 0)) continue;
+        const long long per_cta = (long long)decode_smem_bytes(c, M, K, G, sym == 0) + 1024;
+        long long per_sm = smem_per_sm > 0 ? smem_per_sm / per_cta : 1;
+        per_sm = std::min(per_sm, (long long)(2048 / (32 * c.NW)));
+        if (grid <= per_sm * sm_count) break;
+    }
     return c;
 }
 

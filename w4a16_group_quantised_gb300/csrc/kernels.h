@@ -21,6 +21,7 @@ struct DeviceInfo {
     int device;
     int sm_count;
     int max_smem_optin;
+    int smem_per_sm;        // shared memory of one SM (all resident CTAs together)
     int *status;            // device address of the status word
     void *encode_tiled;     // cuTensorMapEncodeTiled entry point
     float *sk_ws;           // balanced decode kernel: partial sums
@@ -42,7 +43,7 @@ struct DecodeCfg {
     int NS;   // ring stages (2..8)
     int S;    // CTAs along K in a cluster (1..8)
 };
-DecodeCfg decode_pick_cfg(int M, int N, int K, int G, int sym, int dtype, int sm_count);
+DecodeCfg decode_pick_cfg(int M, int N, int K, int G, int sym, int dtype, int sm_count, int smem_per_sm);
 bool decode_cfg_valid(const DecodeCfg &c, int M, int K, int G, bool asym);
 size_t decode_smem_bytes(const DecodeCfg &c, int M, int K, int G, bool asym);
 cudaError_t launch_decode(const GemmArgs &a, const DecodeCfg &c, const DeviceInfo &dev,
