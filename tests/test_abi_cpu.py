@@ -125,6 +125,12 @@ def test_debug_config_validation(lib):
     assert lib.w4a16_debug_set_config(2, arr, 4) == -9   # rings do not fit in shared memory
     arr = (ctypes.c_int * 4)(128, 3, 2, 2)
     assert lib.w4a16_debug_set_config(2, arr, 4) == 0
+    arr = (ctypes.c_int * 5)(128, 3, 2, 2, 8)
+    assert lib.w4a16_debug_set_config(2, arr, 5) == 0    # K split over 8 CTAs
+    arr = (ctypes.c_int * 5)(128, 3, 2, 2, 9)
+    assert lib.w4a16_debug_set_config(2, arr, 5) == -9   # more than 8 CTAs
+    arr = (ctypes.c_int * 5)(256, 3, 2, 2, 2)
+    assert lib.w4a16_debug_set_config(2, arr, 5) == -9   # 256 KB partial tile does not fit
     assert lib.w4a16_debug_set_config(2, None, 0) == 0
     assert lib.w4a16_debug_set_config(9, None, 0) == -9
     # per-warp-stream decode kernel: {mode} or {2, NBK, S, NW, NSW}

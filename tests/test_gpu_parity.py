@@ -203,3 +203,45 @@ def test_host_buffer_entry_point(cuda_lib):
 def test_device_status_clean(cuda_lib):
     torch.cuda.synchronize()
     assert cuda_lib.w4a16_last_device_error() == 0
+
+
+@pytest.mark.parametrize("dtype", [0, 1])
+@pytest.mark.parametrize("sym", [True, False])
+def test_prefill_k_split_integer_exact(cuda_lib, dtype, sym):
+    """Few output tiles: the prefill kernel splits K over a cluster of 2 to 8
+    CTAs (whole 256-k weight tiles each, uneven shares, a ragged K tail in
+    the last one) and sums the partial tiles across the cluster.  s = 1 and
+    integer x make every partial sum exact: bit-exact outputs, twice in a row."""
+    w = cuda_lib
+    cases = [(16, 256, 512, 32), (37, 200, 768, 64), (100, 256, 1184, 32),
+             (64, 512, 2560, 128), (129, 1000, 4096, 128), (48, 2056, 1344, 64)]
+    for (M, N, K, G) in cases:
+        p = make_problem(M, N, K, G, sym, dtype, seed=900 + M + N, x_kind="int4")
+        p.scales[:] = 0x3C00 if dtype == 0 else 0x3F80
+        d = to_device(p, w)
+        y_ref = oracle.gemm(p.x, M, K, d["ref_qw"], p.scales, d["ref_qz"], G, N, dtype)
+        want = oracle.round_array(y_ref, dtype)
+        for _ in range(2):
+            out = w.w4a16_gemm(d["x"], d["qweight"], d["scales"], d["qzeros"], G, path=PREFILL)
+            assert np.array_equal(tensor_to_bits(out), want), (M, N, K, G)
+    assert w.w4a16_last_device_error() == 0
+
+
+@pytest.mark.parametrize("ks", [1, 2, 4, 7, 8])
+def test_prefill_forced_k_split(cuda_lib, ks):
+    """Every cluster size gives the same bit-exact integer result (nine 256-k
+    weight tiles: shares of one to five tiles; ragged M and N)."""
+    w = cuda_lib
+    M, N, K, G = 61, 520, 2304, 64
+    p = make_problem(M, N, K, G, False, 1, seed=4242, x_kind="int4")
+    p.scales[:] = 0x3F80
+    d = to_device(p, w)
+    want = oracle.round_array(oracle.gemm(p.x, M, K, d["ref_qw"], p.scales, d["ref_qz"], G, N, 1), 1)
+    w.w4a16_debug_set_config(2, [64, 4, 2, 2, ks])
+    try:
+        out = w.w4a16_gemm(d["x"], d["qweight"], d["scales"], d["qzeros"], G, path=PREFILL)
+        torch.cuda.synchronize()
+    finally:
+        w.w4a16_debug_set_config(2, None)
+    assert np.array_equal(tensor_to_bits(out), want)
+    assert w.w4a16_last_device_error() == 0

@@ -205,7 +205,7 @@ def w4a16_select_path(M: int, N: int, K: int, G: int, sym: bool, dtype: int) -> 
 
 def w4a16_debug_set_config(which: int, vals=None) -> None:
     """Tuning hook (see include/w4a16.h): which=1 cluster decode kernel
-    {R, NW, NB, NS, S}; which=2 prefill {BN, x stages, A stages, W stages};
+    {R, NW, NB, NS, S}; which=2 prefill {BN, x stages, A stages, W stages[, KS]};
     which=3 programmatic dependent launch {flag}; which=4 balanced decode
     kernel {on, ring depth}; which=5 per-warp-stream decode kernel {mode} or
     {2, NBK, S, NW, NSW}.  vals=None restores the built-in choice."""

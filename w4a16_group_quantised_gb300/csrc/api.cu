@@ -219,7 +219,7 @@ int run_gemm(const void *x, int M, int K, const int32_t *qw, const void *scales,
         {
             std::lock_guard<std::mutex> lk(g_cfg_mu);
             c = g_prefill_override ? g_prefill_cfg
-                                   : prefill_pick_cfg(M, N, K, G, qz == nullptr, dtype, dev->sm_count);
+                                   : prefill_pick_cfg(M, N, K, G, qz == nullptr, dtype, *dev);
         }
         e = launch_prefill(a, c, *dev, s, g_pdl != 0);
     }
@@ -376,8 +376,8 @@ int w4a16_debug_set_config(int which, const int *vals, int n) {
     }
     if (which == 2) {
         if (n == 0) { g_prefill_override = false; return W4A16_OK; }
-        if (n != 4 || vals == nullptr) return W4A16_ERR_ARG;
-        PrefillCfg c{vals[0], vals[1], vals[2], vals[3]};
+        if ((n != 4 && n != 5) || vals == nullptr) return W4A16_ERR_ARG;
+        PrefillCfg c{vals[0], vals[1], vals[2], vals[3], n == 5 ? vals[4] : 0};
         if (!prefill_cfg_valid(c)) return W4A16_ERR_ARG;
         g_prefill_cfg = c;
         g_prefill_override = true;

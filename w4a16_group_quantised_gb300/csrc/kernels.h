@@ -27,6 +27,7 @@ struct DeviceInfo {
     float *sk_ws;           // balanced decode kernel: partial sums
     int *sk_counters;       // balanced decode kernel: per-row-block tickets (zero between calls)
     int sk_max_rowblocks;   // capacity of sk_counters
+    int prefill_clusters[9];  // prefill kernel: clusters of k CTAs resident at once (k = 1..8)
 };
 
 // ---- pack.cu
@@ -81,11 +82,12 @@ struct PrefillCfg {
     int stages;   // x-tile ring stages (64 k each)
     int astages;  // dequantised-weight ring stages
     int wstages;  // packed-weight ring stages (256 k each)
+    int ks = 0;   // CTAs of a cluster splitting K: 0 = chosen at launch, else 1..8
 };
 bool prefill_cfg_valid(const PrefillCfg &c);
-PrefillCfg prefill_pick_cfg(int M, int N, int K, int G, int sym, int dtype, int sm_count);
+PrefillCfg prefill_pick_cfg(int M, int N, int K, int G, int sym, int dtype, const DeviceInfo &dev);
 cudaError_t launch_prefill(const GemmArgs &a, const PrefillCfg &c, const DeviceInfo &dev,
                            cudaStream_t s, bool pdl);
-cudaError_t prefill_prepare_device(const DeviceInfo &dev);
+cudaError_t prefill_prepare_device(DeviceInfo &dev);
 
 }  // namespace w4a16

@@ -39,6 +39,8 @@
 #include "kernels.h"
 #include "ptx.cuh"
 
+#include <algorithm>
+#include <cooperative_groups.h>
 #include <cuda.h>
 
 namespace w4a16 {
@@ -57,9 +59,11 @@ struct PrefillParams {
     DqConsts dq;          // dequantiser masks / magics, passed as data (see dequant.cuh)
     const uint16_t *scales;
     const int32_t *qz;
+    uint16_t *out;        // y [M, N] (written directly when K is split; else by TMA store)
     int M, N, K, G, ng;
     int BN, SX, SA, SW;
     int n_mtiles;
+    int KS;               // CTAs of a cluster splitting K (1 = no split)
     int *status;
 };
 
@@ -110,10 +114,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int SX = p.SX, SA = p.SA, SW = p.SW;
 
-    const int mt = blockIdx.x % p.n_mtiles;
-    const int nt = blockIdx.x / p.n_mtiles;
+    // With KS > 1 the KS CTAs of a cluster share one output tile, rank r
+    // taking packed-weight tiles [r nwt / KS, (r + 1) nwt / KS) of K.
+    const int KS = p.KS;
+    const int krank = KS > 1 ? (int)cluster_ctarank() : 0;
+    const int tile = (int)blockIdx.x / KS;
+    const int mt = tile % p.n_mtiles;
+    const int nt = tile / p.n_mtiles;
     const int m0 = mt * p.BN, n0 = nt * kBW;
-    const int nk = (p.K + kBK - 1) / kBK;
+    const int nk_all = (p.K + kBK - 1) / kBK;
+    const int nwt = (p.K + kWK - 1) / kWK;           // packed-weight tiles along K
+    const int js0 = (int)((long long)krank * nwt / KS), js1 = (int)((long long)(krank + 1) * nwt / KS);
+    const int is0 = js0 * kStepsPerW;                // first 64-k step of this CTA
+    const int nk = min(js1 * kStepsPerW, nk_all) - is0;   // steps of this CTA
 
     const uint32_t bar_base = smem_u32(smem + L.bar_off);
     auto xfull = [&](int s) { return bar_base + 8u * s; };
@@ -173,19 +186,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int s = i % SX;
                 if (!mbar_wait_bounded(xempty(s), (uint32_t)((i / SX) & 1) ^ 1u, p.status, abort_flag)) break;
                 mbar_arrive_expect_tx(xfull(s), xtx);
-                tma_load_2d(x_base + (uint32_t)s * p.BN * 128u, &tmap_x, xfull(s), i * kBK, m0);
+                tma_load_2d(x_base + (uint32_t)s * p.BN * 128u, &tmap_x, xfull(s), (is0 + i) * kBK, m0);
             }
         }
     } else if (warp == 3) {
         // ------------------------------------------------------------ weight producer
         // (its own issuing thread: one thread's TMA boxes complete one after another)
         if (lane == 0) {
-            const int nw = (p.K + kWK - 1) / kWK;
+            const int nw = js1 - js0;
             for (int j = 0; j < nw; ++j) {
                 const int sw = j % SW;
                 if (!mbar_wait_bounded(wempty(sw), (uint32_t)((j / SW) & 1) ^ 1u, p.status, abort_flag)) break;
                 mbar_arrive_expect_tx(wfull(sw), (uint32_t)kWTileBytes);
-                tma_load_2d(w_base + (uint32_t)sw * kWTileBytes, &tmap_w, wfull(sw), j * (kWK / 8), n0);
+                tma_load_2d(w_base + (uint32_t)sw * kWTileBytes, &tmap_w, wfull(sw), (js0 + j) * (kWK / 8), n0);
             }
         }
     } else if (warp == 1) {
@@ -290,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         };
-        load_tile_meta(0);
+        load_tile_meta(js0);
 
         // A tile (both halves): half h = r / 128 at h * 16 KB; 128-byte rows,
         // 16-byte chunk c of row r at position c ^ (r % 8) within its 8-row atom.
@@ -352,34 +365,93 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fence_proxy_async_smem();   // each writer: generic -> async proxy
                     __syncwarp();
                     if (lane == 0) mbar_arrive(afull(a));
-                    if (d == 0) load_tile_meta(i / kStepsPerW + 1);
+                    if (d == 0 && js0 + i / kStepsPerW + 1 < js1) load_tile_meta(js0 + i / kStepsPerW + 1);
                 }
             }
         }
 
         // ------------------------------------------------------------ epilogue
         const bool have_acc = ok && mbar_wait_bounded(acc_bar, 0u, p.status, abort_flag);
-        if (have_acc) {
-            tc_fence_after();
-            const int q = warp & 3, h = (warp - 4) >> 2;
-            const int nl = h * kHalf + 32 * q + lane;            // row of the tile
-            const uint32_t tbase = tmem_d + ((uint32_t)(32 * q) << 16) + (uint32_t)(h * 256);
-            uint16_t *stage = reinterpret_cast<uint16_t *>(smem);   // [BN][256], over x/A rings
-            for (int c0 = 0; c0 < p.BN; c0 += 16) {
-                uint32_t v[16];
-                tmem_ld_32x32b_x16(tbase + (uint32_t)c0, v);
+        if (KS > 1) {
+            // K split: this CTA's fp32 partial tile -> part[token][weight row]
+            // over the (idle) rings; summed across the cluster below.
+            if (have_acc) {
+                tc_fence_after();
+                const int q = warp & 3, h = (warp - 4) >> 2;
+                const int nl = h * kHalf + 32 * q + lane;
+                const uint32_t tbase = tmem_d + ((uint32_t)(32 * q) << 16) + (uint32_t)(h * 256);
+                float *part = reinterpret_cast<float *>(smem);
+                for (int c0 = 0; c0 < p.BN; c0 += 16) {
+                    uint32_t v[16];
+                    tmem_ld_32x32b_x16(tbase + (uint32_t)c0, v);
 #pragma unroll
-                for (int jx = 0; jx < 16; ++jx)
-                    stage[(size_t)(c0 + jx) * kBW + nl] = f32_to_dt16<DT>(__uint_as_float(v[jx]));
+                    for (int jx = 0; jx < 16; ++jx) part[(size_t)(c0 + jx) * kBW + nl] = __uint_as_float(v[jx]);
+                }
             }
-            fence_proxy_async_smem();
+        } else {
+            if (have_acc) {
+                tc_fence_after();
+                const int q = warp & 3, h = (warp - 4) >> 2;
+                const int nl = h * kHalf + 32 * q + lane;            // row of the tile
+                const uint32_t tbase = tmem_d + ((uint32_t)(32 * q) << 16) + (uint32_t)(h * 256);
+                uint16_t *stage = reinterpret_cast<uint16_t *>(smem);   // [BN][256], over x/A rings
+                for (int c0 = 0; c0 < p.BN; c0 += 16) {
+                    uint32_t v[16];
+                    tmem_ld_32x32b_x16(tbase + (uint32_t)c0, v);
+#pragma unroll
+                    for (int jx = 0; jx < 16; ++jx)
+                        stage[(size_t)(c0 + jx) * kBW + nl] = f32_to_dt16<DT>(__uint_as_float(v[jx]));
+                }
+                fence_proxy_async_smem();
+            }
+            named_barrier_sync(1, kDeqWarps * 32);
+            if (have_acc && threadIdx.x == 128) {
+                tma_store_2d(&tmap_out, smem_u32(smem), n0, m0);
+                bulk_commit_group();
+                bulk_wait_group_all();
+            }
         }
-        named_barrier_sync(1, kDeqWarps * 32);
-        if (have_acc && threadIdx.x == 128) {
-            tma_store_2d(&tmap_out, smem_u32(smem), n0, m0);
-            bulk_commit_group();
-            bulk_wait_group_all();
+    }
+
+    if (KS > 1) {
+        // Sum the KS partial tiles in rank order (deterministic); rank r
+        // writes token rows [r BN / KS, (r + 1) BN / KS) of the tile.
+        cluster_sync_all();
+        namespace cg = cooperative_groups;
+        cg::cluster_group cluster = cg::this_cluster();
+        float *part = reinterpret_cast<float *>(smem);
+        const float *peer[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) peer[q] = cluster.map_shared_rank(part, q < KS ? q : 0);
+        const int c_lo = (int)((long long)krank * p.BN / KS), c_hi = (int)((long long)(krank + 1) * p.BN / KS);
+        const int n_v = (c_hi - c_lo) * (kBW / 4);      // float4 groups of this CTA's rows
+        const bool vec_out = (p.N & 3) == 0;
+        for (int idx = threadIdx.x; idx < n_v; idx += kThreads) {
+            const int c = c_lo + (idx >> 6), nl = (idx & 63) * 4;
+            const int m = m0 + c, n = n0 + nl;
+            if (m >= p.M || n >= p.N) continue;
+            const size_t off = (size_t)c * kBW + nl;
+            float4 sum = *reinterpret_cast<const float4 *>(peer[0] + off);
+#pragma unroll
+            for (int q = 1; q < 8; ++q) {
+                if (q < KS) {
+                    const float4 t = *reinterpret_cast<const float4 *>(peer[q] + off);
+                    sum.x += t.x; sum.y += t.y; sum.z += t.z; sum.w += t.w;
+                }
+            }
+            const uint16_t o0 = f32_to_dt16<DT>(sum.x), o1 = f32_to_dt16<DT>(sum.y);
+            const uint16_t o2 = f32_to_dt16<DT>(sum.z), o3 = f32_to_dt16<DT>(sum.w);
+            uint16_t *dst = p.out + (size_t)m * p.N + n;
+            if (vec_out && n + 3 < p.N) {
+                *reinterpret_cast<uint2 *>(dst) = make_uint2(o0 | ((uint32_t)o1 << 16), o2 | ((uint32_t)o3 << 16));
+            } else {
+                dst[0] = o0;
+                if (n + 1 < p.N) dst[1] = o1;
+                if (n + 2 < p.N) dst[2] = o2;
+                if (n + 3 < p.N) dst[3] = o3;
+            }
         }
+        cluster_sync_all();   // keep this CTA's partials alive while the others read them
     }
 
     tc_fence_before();
@@ -401,39 +473,89 @@ static bool prefill_cfg_fits(const PrefillCfg &c) {
            prefill_epilogue_fits(c.BN, c.stages, c.astages);
 }
 
-// Pick BN (tokens per tile) to minimise waves x tile time on the SMs, then
-// the deepest x ring that fits.
-PrefillCfg prefill_pick_cfg(int M, int N, int K, int G, int sym, int dtype, int sm_count) {
-    (void)K; (void)G; (void)sym; (void)dtype;
-    const int ntiles_n = (N + kBW - 1) / kBW;
-    int best_bn = 256;
-    double best_cost = 1e30;
-    for (int bn = 256; bn >= 64; bn -= 16) {
-        const int mt = (M + bn - 1) / bn;
-        const long long tiles = (long long)mt * ntiles_n;
-        const long long waves = (tiles + sm_count - 1) / sm_count;
-        // per-tile time ~ bn (tensor-bound) + a fixed part for dequant/pipeline
-        const double cost = (double)waves * (bn + 48);
-        if (cost < best_cost - 1e-9) {
-            best_cost = cost;
-            best_bn = bn;
-        }
-    }
-    PrefillCfg c{best_bn, 3, 2, 2};
-    if (M < best_bn) {
-        c.BN = ((M + 15) / 16) * 16;
-        if (c.BN < 16) c.BN = 16;
-    }
+// A K split sums fp32 partial tiles ([BN][256], 1 KB a token) laid over the rings.
+static bool prefill_split_fits(const PrefillCfg &c) {
+    return (size_t)c.BN * kBW * 4 <= prefill_layout(c.BN, c.stages, c.astages, c.wstages).bar_off;
+}
+
+// Time model of one launch (microseconds, fitted to GB300 timings of this
+// kernel): a CTA spends about 3.16 + 0.00175 BN per 256-k packed-weight
+// tile (the dequantisers set the pace up to BN = 256), 5 more for start-up,
+// pipeline fill and epilogue, and, when K is split, 1 + BN / 64 for the
+// cluster reduction.  CTAs run in waves of what fits on the GPU at once: one
+// CTA per SM, and with a K split whole clusters of KS CTAs, as many as the
+// occupancy query allowed.
+static double prefill_cost(int bn, int ks, long long tiles, int nwt, const DeviceInfo &dev) {
+    const int resident = dev.prefill_clusters[ks];
+    if (resident <= 0) return 1e30;
+    const long long waves = (tiles + resident - 1) / resident;
+    const int per_cta = (nwt + ks - 1) / ks;
+    const double t = per_cta * (3.16 + 0.00175 * bn) + 5.0 + (ks > 1 ? 1.0 + bn / 64.0 : 0.0);
+    return (double)waves * t;
+}
+
+// The deepest x ring that fits (with room for the partial tile when K is split).
+static bool prefill_fit_stages(PrefillCfg &c) {
     for (int sx = 6; sx >= 2; --sx) {
         c.stages = sx;
-        if (prefill_cfg_fits(c)) break;
+        if (prefill_cfg_fits(c) && (c.ks <= 1 || prefill_split_fits(c))) return true;
     }
-    return c;
+    return false;
+}
+
+static int prefill_best_ks(const PrefillCfg &base, long long tiles, int nwt, const DeviceInfo &dev, double *cost) {
+    int best = 1;
+    double best_cost = 1e30;
+    for (int ks = 1; ks <= 8 && ks <= nwt; ++ks) {
+        PrefillCfg c = base;
+        c.ks = ks;
+        if (ks > 1 && !prefill_split_fits(c)) continue;
+        const double t = prefill_cost(c.BN, ks, tiles, nwt, dev);
+        if (t < best_cost * 0.995) {
+            best_cost = t;
+            best = ks;
+        }
+    }
+    if (cost) *cost = best_cost;
+    return best;
+}
+
+// Pick BN (tokens per tile, at most M rounded up to 16) and the K split that
+// minimise the modelled time, then the deepest x ring that fits.
+PrefillCfg prefill_pick_cfg(int M, int N, int K, int G, int sym, int dtype, const DeviceInfo &dev) {
+    (void)G; (void)sym; (void)dtype;
+    const int ntiles_n = (N + kBW - 1) / kBW;
+    const int nwt = (K + kWK - 1) / kWK;
+    const int bn_max = std::min(256, std::max(16, (M + 15) / 16 * 16));
+    PrefillCfg best{bn_max, 2, 2, 2, 1};
+    double best_cost = 1e30;
+    for (int bn = 16; bn <= bn_max; bn += 16) {
+        PrefillCfg c{bn, 2, 2, 2, 1};
+        if (!prefill_fit_stages(c)) continue;
+        const long long tiles = (long long)((M + bn - 1) / bn) * ntiles_n;
+        double t = 0.0;
+        c.ks = 1;
+        // the deepest ring that still leaves room for the partial tile
+        PrefillCfg cs = c;
+        cs.ks = 2;
+        const bool can_split = prefill_fit_stages(cs);
+        if (can_split) c.stages = cs.stages;
+        c.ks = can_split ? prefill_best_ks(c, tiles, nwt, dev, &t) : 1;
+        if (!can_split) t = prefill_cost(bn, 1, tiles, nwt, dev);
+        if (t < best_cost * 0.995) {
+            best_cost = t;
+            best = c;
+        }
+    }
+    prefill_fit_stages(best);
+    return best;
 }
 
 bool prefill_cfg_valid(const PrefillCfg &c) {
     if (c.BN < 16 || c.BN > 256 || c.BN % 16 != 0) return false;
     if (c.stages < 2 || c.astages < 2 || c.wstages < 2) return false;
+    if (c.ks < 0 || c.ks > 8) return false;
+    if (c.ks > 1 && !prefill_split_fits(c)) return false;
     return prefill_cfg_fits(c);
 }
 
@@ -448,8 +570,15 @@ static cudaError_t launch_t(const CUtensorMap &tx, const CUtensorMap &tw, const 
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attrs[1];
+    cudaLaunchAttribute attrs[2];
     int na = 0;
+    if (p.KS > 1) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = p.KS;
+        attrs[na].val.clusterDim.y = 1;
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
     if (pdl) {
         attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attrs[na].val.programmaticStreamSerializationAllowed = 1;
@@ -460,8 +589,37 @@ static cudaError_t launch_t(const CUtensorMap &tx, const CUtensorMap &tw, const 
     return cudaLaunchKernelEx(&cfg, kern, tx, tw, to, p);
 }
 
-cudaError_t prefill_prepare_device(const DeviceInfo &dev) {
-    (void)dev;
+// How many clusters of KS CTAs (KS = 1 .. 8) of the prefill kernel the GPU
+// holds at once, at the largest shared-memory size (every configuration
+// takes more than half an SM's shared memory, so one CTA per SM).
+cudaError_t prefill_prepare_device(DeviceInfo &dev) {
+    const int smem = dev.max_smem_optin;
+    decltype(&prefill_kernel<0, false>) kerns[4] = {
+        prefill_kernel<0, false>, prefill_kernel<0, true>, prefill_kernel<1, false>, prefill_kernel<1, true>};
+    for (auto k : kerns) {
+        const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+    }
+    dev.prefill_clusters[0] = 0;
+    for (int ks = 1; ks <= 8; ++ks) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(ks * 64, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = ks;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kerns[0], &cfg) != cudaSuccess) {
+            (void)cudaGetLastError();
+            n = ks == 1 ? dev.sm_count : 0;
+        }
+        dev.prefill_clusters[ks] = n;
+    }
     return cudaSuccess;
 }
 
@@ -507,6 +665,7 @@ cudaError_t launch_prefill(const GemmArgs &a, const PrefillCfg &c, const DeviceI
     p.dq = dq_consts_seq(a.dtype);
     p.scales = (const uint16_t *)a.scales;
     p.qz = a.qzeros;
+    p.out = (uint16_t *)a.out;
     p.M = a.M;
     p.N = a.N;
     p.K = a.K;
@@ -519,8 +678,18 @@ cudaError_t launch_prefill(const GemmArgs &a, const PrefillCfg &c, const DeviceI
     p.n_mtiles = (a.M + c.BN - 1) / c.BN;
     p.status = dev.status;
     const int n_ntiles = (a.N + kBW - 1) / kBW;
-    const int grid = n_ntiles * p.n_mtiles;
-    const size_t smem = prefill_layout(c.BN, c.stages, c.astages, c.wstages).total;
+    const SmemLayout L = prefill_layout(c.BN, c.stages, c.astages, c.wstages);
+    // Too few output tiles to fill the SMs (small M): split K over a cluster
+    // of KS CTAs, each summing whole packed-weight tiles, as long as every
+    // CTA keeps at least one tile and the fp32 partial tile fits over the rings.
+    const int tiles = n_ntiles * p.n_mtiles;
+    const int nwt = (a.K + kWK - 1) / kWK;
+    int ks = c.ks;
+    if (ks == 0) ks = prefill_best_ks(c, tiles, nwt, dev, nullptr);
+    ks = std::max(1, std::min(ks, nwt));
+    p.KS = ks;
+    const int grid = tiles * ks;
+    const size_t smem = L.total;
     const bool asym = a.qzeros != nullptr;
     if (a.dtype == 0)
         return asym ? launch_t<0, true>(tx, tw, to, p, smem, grid, s, pdl)

@@ -21,6 +21,19 @@ __device__ __forceinline__ unsigned long long globaltimer() {
     return t;
 }
 
+// ---------------------------------------------------------------- clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Full cluster barrier: every thread of every CTA of the cluster arrives
+// (release) and waits (acquire), so shared-memory writes before it are
+// visible to the other CTAs' distributed-shared-memory reads after it.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- loads
 __device__ __forceinline__ uint4 ldg_stream_v4(const void *p) {
     uint4 v;
