@@ -8,12 +8,14 @@
 // section "Upstream's Python side is kept -- and it does NOT work here").
 //
 // Design (GB300-first, not the pages' RDNA kernel):
-//  * A CTA owns RT = 16 * R * NW weight rows and one K slice.  One thread
-//    streams the slice's packed weights through an NS-stage shared-memory
-//    ring with 2-D TMA boxes of RT rows x 128 k (64 bytes a row, so a warp's
-//    16-byte reads of rows g and g+1 fall on disjoint banks); up to
-//    NS * NB boxes are in flight per CTA from the first cycle.  Scales and
-//    zero points of the slice are staged once; x is staged permuted.
+//  * A CTA owns RT = 16 * R * NW weight rows and one K slice.  A producer
+//    warp (warp NW, one thread) streams the slice's packed weights through
+//    an NS-stage shared-memory ring with 2-D TMA boxes of RT rows x 128 k
+//    (64 bytes a row, so a warp's 16-byte reads of rows g and g+1 fall on
+//    disjoint banks); up to NS * NB boxes are in flight per CTA from the
+//    first cycle, and the NW compute warps never issue or wait for a copy
+//    on each other's behalf.  Scales and zero points of the slice are
+//    staged once; x is staged permuted.
 //  * Each warp owns R blocks of 16 rows.  Per 128-wide K step a lane takes
 //    4 words (32 weights) of rows g and g+8, dequantises them in registers
 //    (dq_word_i4) and multiplies on the tensor cores with mma.sync m16n8k16
@@ -67,8 +69,11 @@ struct DecodeSmem {
 
 // meta: per (row, group) of the slice, {s2} (symmetric) or {s2, zl2}
 // (asymmetric) -- the packed scale and low-magic zero constant, built once.
+// red: the partial sums, [RT][8] fp32 without a K split; with one, the
+// cluster's rank-0 CTA gathers every rank's partials there as [S][M][RT].
+// bars: NS full and NS empty barriers, the abort flag, the gather barrier.
 __host__ __device__ inline DecodeSmem decode_layout(int R, int NW, int NB, int NS, int M, int xpitch,
-                                                    int gmax, bool asym) {
+                                                    int gmax, bool asym, int S) {
     const int RT = 16 * R * NW;
     DecodeSmem L;
     uint32_t off = 0;
@@ -79,16 +84,16 @@ __host__ __device__ inline DecodeSmem decode_layout(int R, int NW, int NB, int N
     off = (off + 127u) & ~127u;
     L.x = off;                                      // [M][xpitch]
     off += (uint32_t)M * xpitch;
-    L.red = off;                                    // [RT][8] fp32
-    off += (uint32_t)RT * 8 * 4;
+    L.red = off;
+    off += (uint32_t)RT * 4 * (S > 1 && S * M > 8 ? S * M : 8);
     L.bars = off;
-    off += (uint32_t)2 * NS * 8 + 16;
+    off += (uint32_t)2 * NS * 8 + 24;
     L.total = off + 128;                            // slack to align the base to 128
     return L;
 }
 
 template <int DT, bool ASYM, int R, int NB>
-__global__ void __launch_bounds__(256, R == 2 ? 3 : 1) decode_kernel(const __grid_constant__ CUtensorMap tmap_w,
+__global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ CUtensorMap tmap_w,
                                                      const DecodeParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
@@ -101,7 +106,7 @@ __global__ void __launch_bounds__(256, R == 2 ? 3 : 1) decode_kernel(const __gri
     const int tile = blockIdx.x / S;
     const int n_tile0 = tile * RT;
     const int M = p.M, K = p.K, gmax = p.gmax, log2G = p.log2G;
-    const DecodeSmem L = decode_layout(R, NW, NB, NS, M, p.xpitch, gmax, ASYM);
+    const DecodeSmem L = decode_layout(R, NW, NB, NS, M, p.xpitch, gmax, ASYM, S);
 
     grid_dependents_launch();
 
@@ -119,6 +124,7 @@ __global__ void __launch_bounds__(256, R == 2 ? 3 : 1) decode_kernel(const __gri
     const uint32_t stage_bytes = (uint32_t)NB * RT * kBoxRowBytes;
     const uint32_t bar0 = sbase + L.bars;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.bars + 16 * NS);
+    const uint32_t gbar = bar0 + 16u * NS + 8u;
 
     auto issue = [&](int step) {  // one thread: TMA all boxes of a ring stage
         const uint32_t sfull = bar0 + 8u * (uint32_t)(step % NS);
@@ -134,185 +140,219 @@ __global__ void __launch_bounds__(256, R == 2 ? 3 : 1) decode_kernel(const __gri
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(bar0 + 8u * s, 1);               // full
-            mbar_init(bar0 + 8u * (NS + s), NW);       // empty: one arrive per warp
+            mbar_init(bar0 + 8u * (NS + s), NW);       // empty: one arrive per compute warp
         }
+        if (S > 1) mbar_init(gbar, S - 1);            // gather: one arrive per other rank
         *abort_flag = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&tmap_w);
-        for (int st = 0; st < min(NS, nsteps); ++st) issue(st);
-    }
-
-    // ---- per-(row, group) constants of the slice (static: before the dependency wait).
-    // RT is a power of two and the CTA has 2 / R threads per row; each thread
-    // walks its row's groups with that stride, four loads in flight at a time.
-    constexpr int kES = ASYM ? 8 : 4;                // meta entry: {s2} or {s2, zl2}
-    {
-        const int tpr = (int)blockDim.x / RT;
-        const int r = (int)threadIdx.x & (RT - 1), gs = (int)threadIdx.x / RT;
-        const int n = n_tile0 + r;
-        const bool vr = n < p.N;
-        const uint16_t *srow = p.scales + (size_t)(vr ? n : 0) * p.ng + g0;
-        const int32_t *zrow = ASYM ? p.qz + (size_t)((vr ? n : 0) >> 3) * p.ng + g0 : nullptr;
-        const int zsh = 4 * (n & 7);
-        unsigned char *mw = smem + L.meta + (size_t)r * gmax * kES;
-        for (int gg0 = gs; gg0 < ngs; gg0 += 4 * tpr) {
-            uint32_t sv[4], zv[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int gg = gg0 + j * tpr;
-                sv[j] = 0u;
-                zv[j] = 0x88888888u;
-                if (vr && gg < ngs) {
-                    sv[j] = __ldg(srow + gg);
-                    if (ASYM) zv[j] = (uint32_t)__ldg(zrow + gg);
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int gg = gg0 + j * tpr;
-                if (gg < ngs) {
-                    if (ASYM)
-                        *reinterpret_cast<uint2 *>(mw + gg * 8) =
-                            make_uint2(rep2(sv[j]), zlo2<DT>((zv[j] >> zsh) & 0xFu));
-                    else
-                        *reinterpret_cast<uint32_t *>(mw + gg * 4) = rep2(sv[j]);
-                }
-            }
-        }
-    }
-
-    // ---- x slice -> shared memory, permuted; zero for k >= K
-    grid_dependency_wait();
-    {
-        unsigned char *xs = smem + L.x;
-        const int nch = nb * 16;                   // 16-byte chunks per row
-        const int kbase = b0 * kBoxK;
-        for (int i = threadIdx.x; i < M * nch; i += blockDim.x) {
-            const int m = i / nch, c = i - (i / nch) * nch;
-            const int k = kbase + 8 * c;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (k < K) v = *reinterpret_cast<const uint4 *>(p.x + (size_t)m * K + k);
-            const int b = c >> 4, cc = c & 15;
-            const int pos = b * 16 + (cc & 3) * 4 + (cc >> 2);   // chunk 4t+w stored at 4w+t
-            uint4 o;
-            o.x = __byte_perm(v.x, v.z, 0x5410);  // (x0, x4)
-            o.y = __byte_perm(v.x, v.z, 0x7632);  // (x1, x5)
-            o.z = __byte_perm(v.y, v.w, 0x5410);  // (x2, x6)
-            o.w = __byte_perm(v.y, v.w, 0x7632);  // (x3, x7)
-            *reinterpret_cast<uint4 *>(xs + (size_t)m * p.xpitch + pos * 16) = o;
-        }
     }
     __syncthreads();
+    if (S > 1) cluster_arrive_relaxed();   // rank 0's gather barrier is initialised
 
-    // Independent accumulator chains per row block: four for one block per
-    // warp, two for two (keeps the register count, and so the CTAs per SM,
-    // of the two-block form down).
-    constexpr int NC = R == 1 ? 4 : 2;
-    float acc[R][NC][4];
-#pragma unroll
-    for (int rb = 0; rb < R; ++rb)
-#pragma unroll
-        for (int c = 0; c < NC; ++c)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[rb][c][e] = 0.f;
-
-    // Lanes whose batch column g is >= M read x row 0: their MMA output
-    // columns are never stored, so no zeroing or predication is needed.
-    const unsigned char *xrow = smem + L.x + (g < M ? g : 0) * p.xpitch + t * 16;
-    const int rloc0 = warp * R * 16 + g;             // row of rb = 0 within the tile
-    const unsigned char *mrow = smem + L.meta + rloc0 * gmax * kES;
-    const uint32_t zl_sym = zlo2<DT>(8u), zh_sym = zhi2<DT>(8u);
-    const DqConsts dc = p.dq;
-
-    bool ok = true;
-    int s = 0, ps = NS - 1;                  // ring slot of this step and of the previous one
-    uint32_t par = 0u, ppar = 1u;            // their phase parities
-    for (int step = 0; step < nsteps && ok; ++step) {
-        // refill the slot used one step ago, once every warp has left it
-        if (threadIdx.x == 0 && step > 0 && step - 1 + NS < nsteps) {
-            if (mbar_wait_bounded(bar0 + 8u * (NS + ps), ppar, p.status, abort_flag)) issue(step - 1 + NS);
+    float *red = reinterpret_cast<float *>(smem + L.red);
+    if (warp == NW) {
+        // ------------------------------------------------------------ producer
+        // Step st refills slot st % NS once the compute warps have released
+        // step st - NS from it.
+        if (lane == 0) {
+            tma_prefetch_desc(&tmap_w);
+            for (int st = 0; st < nsteps; ++st) {
+                if (st >= NS &&
+                    !mbar_wait_bounded(bar0 + 8u * (NS + st % NS), (uint32_t)((st / NS - 1) & 1), p.status,
+                                       abort_flag))
+                    break;
+                issue(st);
+            }
         }
-        if (!mbar_wait_bounded(bar0 + 8u * s, par, p.status, abort_flag)) {
-            ok = false;
-            break;
-        }
-        const unsigned char *stage = smem + L.ring + (size_t)s * stage_bytes;
-        const int lb0 = step * NB;
-#pragma unroll
-        for (int j = 0; j < NB; ++j) {
-            const int lb = lb0 + j;                   // slice-local block
-            if (lb < nb) {
-                const int kb = (b0 + lb) * kBoxK;
-                const int gl = min(((kb + 32 * t) >> log2G) - g0, ngs - 1);
-                const unsigned char *xb = xrow + lb * 256;
-                const uint4 xv[4] = {sh_v4(xb), sh_v4(xb + 64), sh_v4(xb + 128), sh_v4(xb + 192)};
-                const unsigned char *box = stage + j * RT * kBoxRowBytes + t * 16 + rloc0 * kBoxRowBytes;
-                const unsigned char *mg = mrow + gl * kES;
-#pragma unroll
-                for (int rb = 0; rb < R; ++rb) {
-                    const uint4 wa = sh_v4(box + rb * 16 * kBoxRowBytes);
-                    const uint4 wb = sh_v4(box + (rb * 16 + 8) * kBoxRowBytes);
-                    const unsigned char *ma = mg + rb * 16 * gmax * kES;
-                    uint32_t s2a, s2b, zla = zl_sym, zlb = zl_sym, zha = zh_sym, zhb = zh_sym;
-                    if (ASYM) {
-                        const uint2 va = sh_v2(ma);
-                        const uint2 vb = sh_v2(ma + 8 * gmax * kES);
-                        s2a = va.x; zla = va.y; zha = zhi_from_zlo<DT>(zla);
-                        s2b = vb.x; zlb = vb.y; zhb = zhi_from_zlo<DT>(zlb);
-                    } else {
-                        s2a = sh_u32(ma);
-                        s2b = sh_u32(ma + 8 * gmax * kES);
+        __syncwarp();
+        grid_dependency_wait();   // before this warp joins the output stores
+        if (S > 1) cluster_wait();
+    } else {
+
+        // ---- per-(row, group) constants of the slice (static: before the dependency wait).
+        // RT is a power of two and the CTA has 2 / R threads per row; each thread
+        // walks its row's groups with that stride, four loads in flight at a time.
+        constexpr int kES = ASYM ? 8 : 4;                // meta entry: {s2} or {s2, zl2}
+        const int nthr = 32 * NW;                        // compute threads
+        {
+            const int tpr = nthr / RT;
+            const int r = (int)threadIdx.x & (RT - 1), gs = (int)threadIdx.x / RT;
+            const int n = n_tile0 + r;
+            const bool vr = n < p.N;
+            const uint16_t *srow = p.scales + (size_t)(vr ? n : 0) * p.ng + g0;
+            const int32_t *zrow = ASYM ? p.qz + (size_t)((vr ? n : 0) >> 3) * p.ng + g0 : nullptr;
+            const int zsh = 4 * (n & 7);
+            unsigned char *mw = smem + L.meta + (size_t)r * gmax * kES;
+            for (int gg0 = gs; gg0 < ngs; gg0 += 4 * tpr) {
+                uint32_t sv[4], zv[4];
+    #pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int gg = gg0 + j * tpr;
+                    sv[j] = 0u;
+                    zv[j] = 0x88888888u;
+                    if (vr && gg < ngs) {
+                        sv[j] = __ldg(srow + gg);
+                        if (ASYM) zv[j] = (uint32_t)__ldg(zrow + gg);
                     }
-                    mac_block<DT, NC>(acc[rb], dc, wa, wb, zla, zha, s2a, zlb, zhb, s2b, xv);
+                }
+    #pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int gg = gg0 + j * tpr;
+                    if (gg < ngs) {
+                        if (ASYM)
+                            *reinterpret_cast<uint2 *>(mw + gg * 8) =
+                                make_uint2(rep2(sv[j]), zlo2<DT>((zv[j] >> zsh) & 0xFu));
+                        else
+                            *reinterpret_cast<uint32_t *>(mw + gg * 4) = rep2(sv[j]);
+                    }
                 }
             }
         }
-        fence_proxy_async_smem();   // this warp's reads of the slot before the copy that refills it
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar0 + 8u * (NS + s));
-        ps = s;
-        ppar = par;
-        if (++s == NS) {
-            s = 0;
-            par ^= 1u;
+
+        // ---- x slice -> shared memory, permuted; zero for k >= K
+        grid_dependency_wait();
+        {
+            unsigned char *xs = smem + L.x;
+            const int nch = nb * 16;                   // 16-byte chunks per row
+            const int kbase = b0 * kBoxK;
+            for (int i = threadIdx.x; i < M * nch; i += nthr) {
+                const int m = i / nch, c = i - (i / nch) * nch;
+                const int k = kbase + 8 * c;
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (k < K) v = *reinterpret_cast<const uint4 *>(p.x + (size_t)m * K + k);
+                const int b = c >> 4, cc = c & 15;
+                const int pos = b * 16 + (cc & 3) * 4 + (cc >> 2);   // chunk 4t+w stored at 4w+t
+                uint4 o;
+                o.x = __byte_perm(v.x, v.z, 0x5410);  // (x0, x4)
+                o.y = __byte_perm(v.x, v.z, 0x7632);  // (x1, x5)
+                o.z = __byte_perm(v.y, v.w, 0x5410);  // (x2, x6)
+                o.w = __byte_perm(v.y, v.w, 0x7632);  // (x3, x7)
+                *reinterpret_cast<uint4 *>(xs + (size_t)m * p.xpitch + pos * 16) = o;
+            }
+        }
+        named_barrier_sync(1, (uint32_t)nthr);
+
+        // Independent accumulator chains per row block: four for one block per
+        // warp, two for two (keeps the register count, and so the CTAs per SM,
+        // of the two-block form down).
+        constexpr int NC = R == 1 ? 4 : 2;
+        float acc[R][NC][4];
+    #pragma unroll
+        for (int rb = 0; rb < R; ++rb)
+    #pragma unroll
+            for (int c = 0; c < NC; ++c)
+    #pragma unroll
+                for (int e = 0; e < 4; ++e) acc[rb][c][e] = 0.f;
+
+        // Lanes whose batch column g is >= M read x row 0: their MMA output
+        // columns are never stored, so no zeroing or predication is needed.
+        const unsigned char *xrow = smem + L.x + (g < M ? g : 0) * p.xpitch + t * 16;
+        const int rloc0 = warp * R * 16 + g;             // row of rb = 0 within the tile
+        const unsigned char *mrow = smem + L.meta + rloc0 * gmax * kES;
+        const uint32_t zl_sym = zlo2<DT>(8u), zh_sym = zhi2<DT>(8u);
+        const DqConsts dc = p.dq;
+
+        bool ok = true;
+        int s = 0;                               // ring slot of this step
+        uint32_t par = 0u;                       // its phase parity
+        for (int step = 0; step < nsteps && ok; ++step) {
+            if (!mbar_wait_bounded(bar0 + 8u * s, par, p.status, abort_flag)) {
+                ok = false;
+                break;
+            }
+            const unsigned char *stage = smem + L.ring + (size_t)s * stage_bytes;
+            const int lb0 = step * NB;
+    #pragma unroll
+            for (int j = 0; j < NB; ++j) {
+                const int lb = lb0 + j;                   // slice-local block
+                if (lb < nb) {
+                    const int kb = (b0 + lb) * kBoxK;
+                    const int gl = min(((kb + 32 * t) >> log2G) - g0, ngs - 1);
+                    const unsigned char *xb = xrow + lb * 256;
+                    const uint4 xv[4] = {sh_v4(xb), sh_v4(xb + 64), sh_v4(xb + 128), sh_v4(xb + 192)};
+                    const unsigned char *box = stage + j * RT * kBoxRowBytes + t * 16 + rloc0 * kBoxRowBytes;
+                    const unsigned char *mg = mrow + gl * kES;
+    #pragma unroll
+                    for (int rb = 0; rb < R; ++rb) {
+                        const uint4 wa = sh_v4(box + rb * 16 * kBoxRowBytes);
+                        const uint4 wb = sh_v4(box + (rb * 16 + 8) * kBoxRowBytes);
+                        const unsigned char *ma = mg + rb * 16 * gmax * kES;
+                        uint32_t s2a, s2b, zla = zl_sym, zlb = zl_sym, zha = zh_sym, zhb = zh_sym;
+                        if (ASYM) {
+                            const uint2 va = sh_v2(ma);
+                            const uint2 vb = sh_v2(ma + 8 * gmax * kES);
+                            s2a = va.x; zla = va.y; zha = zhi_from_zlo<DT>(zla);
+                            s2b = vb.x; zlb = vb.y; zhb = zhi_from_zlo<DT>(zlb);
+                        } else {
+                            s2a = sh_u32(ma);
+                            s2b = sh_u32(ma + 8 * gmax * kES);
+                        }
+                        mac_block<DT, NC>(acc[rb], dc, wa, wb, zla, zha, s2a, zlb, zhb, s2b, xv);
+                    }
+                }
+            }
+            fence_proxy_async_smem();   // this warp's reads of the slot before the copy that refills it
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar0 + 8u * (NS + s));
+            if (++s == NS) {
+                s = 0;
+                par ^= 1u;
+            }
+        }
+
+        // ---- partial sums -> shared memory: red[row][m]
+        if (S == 1) {
+#pragma unroll
+            for (int rb = 0; rb < R; ++rb) {
+                const int r0 = (warp * R + rb) * 16;
+                red[(r0 + g) * 8 + 2 * t] = chain_sum(acc[rb], 0);
+                red[(r0 + g) * 8 + 2 * t + 1] = chain_sum(acc[rb], 1);
+                red[(r0 + g + 8) * 8 + 2 * t] = chain_sum(acc[rb], 2);
+                red[(r0 + g + 8) * 8 + 2 * t + 1] = chain_sum(acc[rb], 3);
+            }
+        } else {
+            // partials of the real batch columns into slot `rank` of rank 0's
+            // gather buffer, [S][M][RT]
+            cluster_wait();
+            const uint32_t gbase = mapa_shared(smem_u32(red), 0u) + (uint32_t)rank * M * RT * 4u;
+#pragma unroll
+            for (int rb = 0; rb < R; ++rb) {
+                const int r0 = (warp * R + rb) * 16;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int row = r0 + g + (e >= 2 ? 8 : 0), col = 2 * t + (e & 1);
+                    if (col < M) st_cluster_f32(gbase + (uint32_t)(col * RT + row) * 4u, chain_sum(acc[rb], e));
+                }
+            }
+            fence_acq_rel_cluster();
         }
     }
 
-    // ---- partial sums -> shared memory: red[row][m]
-    float *red = reinterpret_cast<float *>(smem + L.red);
-#pragma unroll
-    for (int rb = 0; rb < R; ++rb) {
-        const int r0 = (warp * R + rb) * 16;
-        red[(r0 + g) * 8 + 2 * t] = chain_sum(acc[rb], 0);
-        red[(r0 + g) * 8 + 2 * t + 1] = chain_sum(acc[rb], 1);
-        red[(r0 + g + 8) * 8 + 2 * t] = chain_sum(acc[rb], 2);
-        red[(r0 + g + 8) * 8 + 2 * t + 1] = chain_sum(acc[rb], 3);
-    }
-    if (S > 1) {
-        cg::this_cluster().sync();
-    } else {
+    if (S == 1) {
         __syncthreads();
-    }
-
-    // ---- reduce over the S cluster ranks; rank r writes its share of outputs
-    {
-        const int total = RT * M;
-        const int i0 = (int)((long long)rank * total / S);
-        const int i1 = (int)((long long)(rank + 1) * total / S);
-        for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
+        for (int i = threadIdx.x; i < RT * M; i += blockDim.x) {
+            const int m = i / RT, row = i - (i / RT) * RT;
+            const int n = n_tile0 + row;
+            if (n < p.N) p.out[(size_t)m * p.N + n] = f32_to_dt<DT>(red[row * 8 + m]);
+        }
+    } else if (rank != 0) {
+        // every partial of this CTA is stored: tell rank 0, and leave
+        __syncthreads();
+        if (threadIdx.x == 0) mbar_arrive_remote(mapa_shared(gbar, 0u));
+    } else {
+        // rank 0: own partials (this CTA) and the other ranks' (gather
+        // barrier), then the sum over ranks in rank order
+        __syncthreads();
+        mbar_wait_cluster_bounded(gbar, 0u, p.status, abort_flag);
+        for (int i = threadIdx.x; i < RT * M; i += blockDim.x) {
             const int m = i / RT, row = i - (i / RT) * RT;
             const int n = n_tile0 + row;
             if (n >= p.N) continue;
-            const int off = row * 8 + m;
-            float sum = 0.f;
-            for (int s = 0; s < S; ++s) {
-                const float *rs = (S > 1) ? cg::this_cluster().map_shared_rank(red, s) : red;
-                sum += rs[off];
-            }
+            float sum = red[m * RT + row];
+            for (int q = 1; q < S; ++q) sum += red[(q * M + m) * RT + row];
             p.out[(size_t)m * p.N + n] = f32_to_dt<DT>(sum);
         }
     }
-    if (S > 1) cg::this_cluster().sync();  // keep shared memory alive for readers
 }
 
 // ------------------------------------------------------------------ host side
@@ -336,7 +376,7 @@ static int decode_xpitch(const DecodeCfg &c, int K) {
 }
 
 size_t decode_smem_bytes(const DecodeCfg &c, int M, int K, int G, bool asym) {
-    return decode_layout(c.R, c.NW, c.NB, c.NS, M, decode_xpitch(c, K), decode_gmax(c, K, G), asym).total;
+    return decode_layout(c.R, c.NW, c.NB, c.NS, M, decode_xpitch(c, K), decode_gmax(c, K, G), asym, c.S).total;
 }
 
 bool decode_cfg_valid(const DecodeCfg &c, int M, int K, int G, bool asym) {
@@ -380,7 +420,7 @@ DecodeCfg decode_pick_cfg(int M, int N, int K, int G, int sym, int dtype, int sm
         if (!decode_cfg_valid(c, M, K, G, sym == 0)) continue;
         const long long per_cta = (long long)decode_smem_bytes(c, M, K, G, sym == 0) + 1024;
         long long per_sm = smem_per_sm > 0 ? smem_per_sm / per_cta : 1;
-        per_sm = std::min(per_sm, (long long)(2048 / (32 * c.NW)));
+        per_sm = std::min(per_sm, (long long)(2048 / (32 * (c.NW + 1))));
         if (grid <= per_sm * sm_count) break;
     }
     return c;
@@ -396,7 +436,7 @@ static cudaError_t launch_t(const CUtensorMap &tw, const DecodeParams &p, const 
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
-    cfg.blockDim = dim3(32 * c.NW, 1, 1);
+    cfg.blockDim = dim3(32 * (c.NW + 1), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attrs[2];
