@@ -142,9 +142,10 @@ __global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ 
             mbar_init(bar0 + 8u * s, 1);               // full
             mbar_init(bar0 + 8u * (NS + s), NW);       // empty: one arrive per compute warp
         }
-        if (S > 1) mbar_init(gbar, S - 1);            // gather: one arrive per other rank
+        if (S > 1) mbar_init(gbar, 1);                // gather: rank 0's own arrive + the others' bytes
         *abort_flag = 0;
         fence_mbar_init();
+        if (S > 1 && rank == 0) mbar_arrive_expect_tx(gbar, (uint32_t)(S - 1) * M * RT * 4u);
     }
     __syncthreads();
     if (S > 1) cluster_arrive_relaxed();   // rank 0's gather barrier is initialised
@@ -312,19 +313,25 @@ __global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ 
             }
         } else {
             // partials of the real batch columns into slot `rank` of rank 0's
-            // gather buffer, [S][M][RT]
+            // gather buffer, [S][M][RT]: rank 0 plainly, the others with
+            // asynchronous stores counted by rank 0's gather barrier
             cluster_wait();
             const uint32_t gbase = mapa_shared(smem_u32(red), 0u) + (uint32_t)rank * M * RT * 4u;
+            const uint32_t gbar0 = mapa_shared(gbar, 0u);
 #pragma unroll
             for (int rb = 0; rb < R; ++rb) {
                 const int r0 = (warp * R + rb) * 16;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int row = r0 + g + (e >= 2 ? 8 : 0), col = 2 * t + (e & 1);
-                    if (col < M) st_cluster_f32(gbase + (uint32_t)(col * RT + row) * 4u, chain_sum(acc[rb], e));
+                    if (col < M) {
+                        if (rank == 0)
+                            red[col * RT + row] = chain_sum(acc[rb], e);
+                        else
+                            st_async_f32(gbase + (uint32_t)(col * RT + row) * 4u, chain_sum(acc[rb], e), gbar0);
+                    }
                 }
             }
-            fence_acq_rel_cluster();
         }
     }
 
@@ -335,13 +342,9 @@ __global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ 
             const int n = n_tile0 + row;
             if (n < p.N) p.out[(size_t)m * p.N + n] = f32_to_dt<DT>(red[row * 8 + m]);
         }
-    } else if (rank != 0) {
-        // every partial of this CTA is stored: tell rank 0, and leave
-        __syncthreads();
-        if (threadIdx.x == 0) mbar_arrive_remote(mapa_shared(gbar, 0u));
-    } else {
-        // rank 0: own partials (this CTA) and the other ranks' (gather
-        // barrier), then the sum over ranks in rank order
+    } else if (rank == 0) {
+        // rank 0: own partials (this CTA) and the other ranks' (their bytes
+        // complete the gather barrier), then the sum over ranks in rank order
         __syncthreads();
         mbar_wait_cluster_bounded(gbar, 0u, p.status, abort_flag);
         for (int i = threadIdx.x; i < RT * M; i += blockDim.x) {
