@@ -59,8 +59,19 @@ struct DecodeParams {
     int M, N, K, G, ng, log2G;
     int NW, NB, NS, S;
     int nblk;        // K blocks of 128 (the last one may be partial)
+    int wide;        // K % 128 == 0: full stages come in one copy (maps.wide)
     int xpitch;      // bytes per x row in shared memory
     int gmax;        // max groups per CTA slice
+};
+
+// Weight tensor maps: `one` loads one 128-k block of RT rows (2-D, exact
+// bounds); `wide` loads NB consecutive blocks in one copy (a 3-D view of the
+// rows as [blocks][row][16 words], only when K is a multiple of 128, so that
+// no block runs past the end of a row).  Fewer, larger copies per stage keep
+// the producer thread's copy issue off the critical path.
+struct DecodeMaps {
+    CUtensorMap one;
+    CUtensorMap wide;
 };
 
 struct DecodeSmem {
@@ -93,7 +104,7 @@ __host__ __device__ inline DecodeSmem decode_layout(int R, int NW, int NB, int N
 }
 
 template <int DT, bool ASYM, int R, int NB>
-__global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ CUtensorMap tmap_w,
+__global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ DecodeMaps maps,
                                                      const DecodeParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
@@ -132,9 +143,13 @@ __global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ 
         const int bb = b0 + step * NB;
         const int nbox = min(NB, b1 - bb);
         mbar_arrive_expect_tx(sfull, (uint32_t)nbox * RT * kBoxRowBytes);
-        for (int j = 0; j < nbox; ++j)
-            tma_load_2d(sdst + (uint32_t)j * RT * kBoxRowBytes, &tmap_w, sfull, (bb + j) * (kBoxK / 8),
-                        n_tile0);
+        if (p.wide && nbox == NB) {
+            tma_load_3d(sdst, &maps.wide, sfull, 0, n_tile0, bb);
+        } else {
+            for (int j = 0; j < nbox; ++j)
+                tma_load_2d(sdst + (uint32_t)j * RT * kBoxRowBytes, &maps.one, sfull, (bb + j) * (kBoxK / 8),
+                            n_tile0);
+        }
     };
 
     if (threadIdx.x == 0) {
@@ -156,7 +171,8 @@ __global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ 
         // Step st refills slot st % NS once the compute warps have released
         // step st - NS from it.
         if (lane == 0) {
-            tma_prefetch_desc(&tmap_w);
+            tma_prefetch_desc(&maps.one);
+            if (p.wide) tma_prefetch_desc(&maps.wide);
             for (int st = 0; st < nsteps; ++st) {
                 if (st >= NS &&
                     !mbar_wait_bounded(bar0 + 8u * (NS + st % NS), (uint32_t)((st / NS - 1) & 1), p.status,
@@ -430,7 +446,7 @@ DecodeCfg decode_pick_cfg(int M, int N, int K, int G, int sym, int dtype, int sm
 }
 
 template <int DT, bool ASYM, int R, int NB>
-static cudaError_t launch_t(const CUtensorMap &tw, const DecodeParams &p, const DecodeCfg &c,
+static cudaError_t launch_t(const DecodeMaps &tw, const DecodeParams &p, const DecodeCfg &c,
                             size_t smem, cudaStream_t s, bool pdl, int grid) {
     auto kern = decode_kernel<DT, ASYM, R, NB>;
     if (smem > 48 * 1024) {
@@ -462,7 +478,7 @@ static cudaError_t launch_t(const CUtensorMap &tw, const DecodeParams &p, const 
 }
 
 template <int DT, bool ASYM>
-static cudaError_t launch_rnb(int R, int NB, const CUtensorMap &tw, const DecodeParams &p,
+static cudaError_t launch_rnb(int R, int NB, const DecodeMaps &tw, const DecodeParams &p,
                               const DecodeCfg &c, size_t smem, cudaStream_t s, bool pdl, int grid) {
     if (R == 1) {
         switch (NB) {
@@ -478,7 +494,7 @@ static cudaError_t launch_rnb(int R, int NB, const CUtensorMap &tw, const Decode
     }
 }
 
-static cudaError_t launch_dispatch(int dtype, bool asym, int R, int NB, const CUtensorMap &tw,
+static cudaError_t launch_dispatch(int dtype, bool asym, int R, int NB, const DecodeMaps &tw,
                                    const DecodeParams &p, const DecodeCfg &c, size_t smem,
                                    cudaStream_t s, bool pdl, int grid) {
     if (dtype == 0)
@@ -493,17 +509,29 @@ cudaError_t launch_decode(const GemmArgs &a, const DecodeCfg &c, const DeviceInf
     if (dev.encode_tiled == nullptr) return cudaErrorNotSupported;
     const bool asym = a.qzeros != nullptr;
     const int RT = 16 * c.R * c.NW;
-    CUtensorMap tw;
+    DecodeMaps tw;
+    const bool wide = a.K % kBoxK == 0;
     {
         EncodeTiledFn encode = reinterpret_cast<EncodeTiledFn>(dev.encode_tiled);
         cuuint64_t dims[2] = {(cuuint64_t)(a.K / 8), (cuuint64_t)a.N};
         cuuint64_t strides[1] = {(cuuint64_t)(a.K / 8) * 4};
         cuuint32_t box[2] = {(cuuint32_t)(kBoxK / 8), (cuuint32_t)RT};
         cuuint32_t estr[2] = {1, 1};
-        CUresult r = encode(&tw, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<int32_t *>(a.qweight), dims,
+        CUresult r = encode(&tw.one, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<int32_t *>(a.qweight), dims,
                             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+        tw.wide = tw.one;
+        if (wide) {
+            cuuint64_t dims3[3] = {(cuuint64_t)(kBoxK / 8), (cuuint64_t)a.N, (cuuint64_t)(a.K / kBoxK)};
+            cuuint64_t strides3[2] = {(cuuint64_t)(a.K / 8) * 4, (cuuint64_t)kBoxRowBytes};
+            cuuint32_t box3[3] = {(cuuint32_t)(kBoxK / 8), (cuuint32_t)RT, (cuuint32_t)c.NB};
+            cuuint32_t estr3[3] = {1, 1, 1};
+            r = encode(&tw.wide, CU_TENSOR_MAP_DATA_TYPE_INT32, 3, const_cast<int32_t *>(a.qweight), dims3,
+                       strides3, box3, estr3, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+        }
     }
     DecodeParams p;
     p.x = (const uint16_t *)a.x;
@@ -523,6 +551,7 @@ cudaError_t launch_decode(const GemmArgs &a, const DecodeCfg &c, const DeviceInf
     p.NS = c.NS;
     p.S = c.S;
     p.nblk = (a.K + kBoxK - 1) / kBoxK;
+    p.wide = wide ? 1 : 0;
     p.xpitch = decode_xpitch(c, a.K);
     p.gmax = decode_gmax(c, a.K, a.G);
     const int tiles = (a.N + RT - 1) / RT;
