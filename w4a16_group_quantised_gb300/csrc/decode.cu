@@ -423,9 +423,9 @@ DecodeCfg decode_pick_cfg(int M, int N, int K, int G, int sym, int dtype, int sm
     if (N >= 24576)
         c = DecodeCfg{1, 4, 4, 2, 1};
     else if (N >= 16384)
-        c = DecodeCfg{1, 8, 2, 2, 2};
+        c = DecodeCfg{1, 8, 2, 3, 2};
     else if (N >= 6144)
-        c = DecodeCfg{1, 4, 4, 4, 4};
+        c = DecodeCfg{1, 4, 4, 2, 5};
     else
         c = DecodeCfg{1, 4, 4, 4, 8};
     const int nblk = (K + kBoxK - 1) / kBoxK;
