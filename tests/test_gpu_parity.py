@@ -245,3 +245,29 @@ def test_prefill_forced_k_split(cuda_lib, ks):
         w.w4a16_debug_set_config(2, None)
     assert np.array_equal(tensor_to_bits(out), want)
     assert w.w4a16_last_device_error() == 0
+
+
+DECODE_FORCED = [[1, 4, 4, 2, 5], [1, 8, 2, 3, 2], [2, 4, 2, 2, 3], [1, 4, 4, 4, 8], [1, 2, 4, 3, 7], [2, 8, 1, 2, 2]]
+
+
+@pytest.mark.parametrize("cfg", DECODE_FORCED, ids=lambda c: "-".join(map(str, c)))
+@pytest.mark.parametrize("sym", [True, False])
+def test_decode_forced_config_integer_exact(cuda_lib, cfg, sym):
+    """Every decode configuration family, forced through the tuning hook,
+    gives the oracle's result bit for bit on integer-exact inputs (ragged N
+    and K tails, cluster sizes 1 to 8, one or two row blocks per warp, one to
+    four boxes per stage, M up to 8)."""
+    w = cuda_lib
+    for (M, N, K, G) in [(1, 264, 2560, 128), (3, 1000, 1184, 32), (8, 520, 4096, 64)]:
+        p = make_problem(M, N, K, G, sym, 1, seed=7100 + M + N, x_kind="int4")
+        p.scales[:] = 0x3F80
+        d = to_device(p, w)
+        want = oracle.round_array(oracle.gemm(p.x, M, K, d["ref_qw"], p.scales, d["ref_qz"], G, N, 1), 1)
+        w.w4a16_debug_set_config(1, cfg)
+        try:
+            out = w.w4a16_gemm(d["x"], d["qweight"], d["scales"], d["qzeros"], G, path=DECODE)
+            torch.cuda.synchronize()
+        finally:
+            w.w4a16_debug_set_config(1, None)
+        assert np.array_equal(tensor_to_bits(out), want), (cfg, M, N, K, G)
+    assert w.w4a16_last_device_error() == 0
