@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ 
             unsigned char *mw = smem + L.meta + (size_t)r * gmax * kES;
             for (int gg0 = gs; gg0 < ngs; gg0 += 4 * tpr) {
                 uint32_t sv[4], zv[4];
-    #pragma unroll
+#pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int gg = gg0 + j * tpr;
                     sv[j] = 0u;
@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ 
                         if (ASYM) zv[j] = (uint32_t)__ldg(zrow + gg);
                     }
                 }
-    #pragma unroll
+#pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int gg = gg0 + j * tpr;
                     if (gg < ngs) {
@@ -254,11 +254,11 @@ __global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ 
         // of the two-block form down).
         constexpr int NC = R == 1 ? 4 : 2;
         float acc[R][NC][4];
-    #pragma unroll
+#pragma unroll
         for (int rb = 0; rb < R; ++rb)
-    #pragma unroll
+#pragma unroll
             for (int c = 0; c < NC; ++c)
-    #pragma unroll
+#pragma unroll
                 for (int e = 0; e < 4; ++e) acc[rb][c][e] = 0.f;
 
         // Lanes whose batch column g is >= M read x row 0: their MMA output
@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ 
             }
             const unsigned char *stage = smem + L.ring + (size_t)s * stage_bytes;
             const int lb0 = step * NB;
-    #pragma unroll
+#pragma unroll
             for (int j = 0; j < NB; ++j) {
                 const int lb = lb0 + j;                   // slice-local block
                 if (lb < nb) {
@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ 
                     const uint4 xv[4] = {sh_v4(xb), sh_v4(xb + 64), sh_v4(xb + 128), sh_v4(xb + 192)};
                     const unsigned char *box = stage + j * RT * kBoxRowBytes + t * 16 + rloc0 * kBoxRowBytes;
                     const unsigned char *mg = mrow + gl * kES;
-    #pragma unroll
+#pragma unroll
                     for (int rb = 0; rb < R; ++rb) {
                         const uint4 wa = sh_v4(box + rb * 16 * kBoxRowBytes);
                         const uint4 wb = sh_v4(box + (rb * 16 + 8) * kBoxRowBytes);
