@@ -23,9 +23,13 @@
 //    columns, rows >= M are zero).  The k order inside an MMA is a
 //    permutation of each word's nibbles; x is staged in the same
 //    permutation, so the dot product is the plain one.
-//  * Split-K across the S CTAs of a thread-block cluster: partial sums meet
-//    in shared memory and are reduced through distributed shared memory in
-//    a fixed order (deterministic, no global workspace, no atomics).
+//  * Split-K across the S CTAs of a thread-block cluster: ranks 1..S-1 send
+//    their fp32 partials (real batch columns only) into rank 0's shared
+//    memory with st.async, whose bytes complete rank 0's gather barrier, and
+//    leave; rank 0 sums the S partials in rank order and stores y
+//    (deterministic, no global workspace, no atomics, no cluster barrier at
+//    the end).  A full ring stage arrives in one 3-D TMA copy when K is a
+//    multiple of 128.
 //  * Programmatic dependent launch: weights, scales and zero points are
 //    requested before the grid-dependency wait; x and out are touched only
 //    after it.  Weights, scales and zero points must therefore not be

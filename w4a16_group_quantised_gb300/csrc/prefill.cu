@@ -32,6 +32,14 @@
 //    single-thread MMA issuer (tcgen05.mma.cta_group::1.kind::f16,
 //    128 x BN x 16 per instruction, two per 16 k); tcgen05.commit releases
 //    ring slots and finally signals the epilogue.
+//  * Few output tiles (small M): K is split over a thread-block cluster of
+//    KS <= 8 CTAs, rank r taking packed-weight tiles [r T / KS, (r+1) T / KS)
+//    of the T along K into its own TMEM accumulator.  The fp32 partial tiles
+//    are laid over the idle rings and summed in rank order through
+//    distributed shared memory, rank r storing token rows [r BN / KS,
+//    (r + 1) BN / KS) of the tile (deterministic; KS = 1 is the plain path).
+//    The host picks BN and KS with a time model fitted to this kernel and
+//    the GPU's cluster occupancy.
 //  * Every mbarrier wait is bounded (%globaltimer); a wait that runs out sets
 //    the device status word and a CTA abort flag, and every role leaves its
 //    loop, so the CTA still frees its TMEM and exits.
