@@ -13,7 +13,7 @@ measured in the same run on the Llama-3.1-8B-shaped asymmetric bf16 G = 64
 layers and reported under "prefill".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-  python bench.py --profile-case decode|prefill --steps K --warmup W   (ncu)
+  python bench.py --profile-case decode|prefill [--profile-m M] --steps K --warmup W   (ncu)
   python bench.py --crossover        (decode vs prefill kernel time, M = 1..16)
 
 --impl reference times the CPU oracle (plain C, fp64) on the same workload
@@ -334,14 +334,16 @@ def bench_prefill(w, steps):
                                   for (ms, (_, N, K)) in zip(per_ms, shapes)])
 
 
-def profile_case(w, which, steps, warmup):
+def profile_case(w, which, steps, warmup, m=None):
     """A short run for ncu captures: `warmup` then `steps` eager passes over
     the four layers of one workload (one set of inputs, launched in layer
-    order).  Prints a timing line of its own, not a bench line."""
+    order); `m` overrides the workload's batch size (prefill: any M, e.g.
+    128 for the K split over a cluster).  Prints a timing line of its own,
+    not a bench line."""
     if which == "decode":
-        layers = [upload(w, wl.qwen3_4b_decode(i, 1)) for i in range(len(wl.QWEN3_4B_SHAPES))]
+        layers = [upload(w, wl.qwen3_4b_decode(i, m or 1)) for i in range(len(wl.QWEN3_4B_SHAPES))]
     else:
-        layers = [upload(w, wl.llama31_8b_prefill(i, 1920)) for i in range(len(wl.LLAMA31_8B_SHAPES))]
+        layers = [upload(w, wl.llama31_8b_prefill(i, m or 1920)) for i in range(len(wl.LLAMA31_8B_SHAPES))]
     td = torch.float16 if layers[0]["dtype"] == 0 else torch.bfloat16
     outs = [torch.empty((d["M"], d["N"]), dtype=td, device="cuda") for d in layers]
     for _ in range(warmup):
@@ -351,7 +353,7 @@ def profile_case(w, which, steps, warmup):
     for _ in range(steps):
         run_step(w, layers, outs)
     torch.cuda.synchronize()
-    print(json.dumps({"profile_case": which, "steps": steps, "warmup": warmup,
+    print(json.dumps({"profile_case": which, "M": layers[0]["M"], "steps": steps, "warmup": warmup,
                       "host_ms_per_step": (time.perf_counter() - t0) / steps * 1e3,
                       "device_status": w.w4a16_last_device_error()}))
 
@@ -432,6 +434,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--profile-case", choices=["decode", "prefill"],
                     help="run only the short eager case that ncu captures")
+    ap.add_argument("--profile-m", type=int, default=None,
+                    help="batch size of the --profile-case workload (default: its own)")
     ap.add_argument("--crossover", action="store_true",
                     help="time both kernels at M = 1..16 (the dispatcher's threshold sweep)")
     args = ap.parse_args()
@@ -466,7 +470,7 @@ def main():
     w.load_library()
 
     if args.profile_case:
-        profile_case(w, args.profile_case, steps, warmup)
+        profile_case(w, args.profile_case, steps, warmup, args.profile_m)
         return
     if args.crossover:
         crossover(w)
