@@ -111,8 +111,7 @@ template <int DT, bool ASYM, int R, int NB>
 __global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ DecodeMaps maps,
                                                      const DecodeParams p) {
     extern __shared__ unsigned char smem_raw[];
-    unsigned char *smem = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~(uintptr_t)127);
+    unsigned char *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
     const int NW = p.NW, NS = p.NS, S = p.S;

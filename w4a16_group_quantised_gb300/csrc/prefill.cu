@@ -116,8 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_out, const PrefillParams p) {
     extern __shared__ unsigned char smem_raw[];
-    unsigned char *smem = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const SmemLayout L = prefill_layout(p.BN, p.SX, p.SA, p.SW);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int SX = p.SX, SA = p.SA, SW = p.SW;
