@@ -423,6 +423,49 @@ def cpu_baseline(sample_steps=None, budget_s=15.0):
                 s_per_step=dt)
 
 
+def reference_arm(steps, warmup, budget_s=150.0):
+    """The oracle (as it stands) on the host cores, over `warmup` untimed and
+    `steps` timed steps of the decode workload.  A whole step (the four
+    layers, every weight row) takes ~0.2 s on the host, so when steps +
+    warmup of them would not fit in `budget_s` each step is a bounded sample:
+    the same contiguous fraction of every layer's weight rows (a multiple of
+    8, at least 8), moving through the rows from step to step.  The metric is
+    bytes streamed per second, so it is the same quantity either way."""
+    import oracle
+    oracle.build()
+    shapes = wl.QWEN3_4B_SHAPES
+    probs = [wl.qwen3_4b_decode(i, 1) for i in range(len(shapes))]
+    packed = [oracle.pack(p.q) for p in probs]
+    t0 = time.perf_counter()
+    for p, qw in zip(probs, packed):
+        oracle.gemm(p.x, p.M, p.K, qw, p.scales, None, p.G, p.N, p.dtype)
+    t_full = time.perf_counter() - t0
+    total = max(1, steps + warmup)
+    frac = min(1.0, budget_s / (total * t_full))
+    nrows = [min(p.N, max(8, int(p.N * frac) // 8 * 8)) for p in probs]
+
+    def one_step(i):
+        nbytes = 0
+        for p, qw, nr in zip(probs, packed, nrows):
+            n0 = (i * nr) % (p.N - nr + 1) // 8 * 8
+            oracle.gemm(p.x, p.M, p.K, qw[n0:n0 + nr], p.scales[n0:n0 + nr], None, p.G, nr, p.dtype)
+            nbytes += decode_bytes(p.M, nr, p.K, p.G, True)
+        return nbytes
+
+    for i in range(warmup):
+        one_step(i)
+    nbytes = 0
+    t0 = time.perf_counter()
+    for i in range(steps):
+        nbytes += one_step(warmup + i)
+    dt = max(time.perf_counter() - t0, 1e-9)
+    sample = (f"each step: rows {nrows} of the four Qwen3-4B-shaped layers "
+              f"(N = {[p.N for p in probs]}), M=1, in fp64 C" if frac < 1.0 else
+              "each step: the whole decode step (4 Qwen3-4B-shaped layers, M=1) in fp64 C")
+    return dict(value=nbytes / dt / 1e9, unit="GB/s", cores=oracle.num_threads(), kind="oracle",
+                sample=sample, s_per_step=dt / max(steps, 1))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -447,9 +490,9 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        cb = cpu_baseline(sample_steps=None, budget_s=12.0)
+        cb = reference_arm(max(args.steps, 1), max(args.warmup, 0))
         line = {"metric": METRIC, "value": round(cb["value"], 4), "unit": "GB/s", "n_gpus": args.gpus,
-                "steps": 1, "warmup": 0, "ms_per_step": cb["s_per_step"] * 1e3,
+                "steps": max(args.steps, 1), "warmup": max(args.warmup, 0), "ms_per_step": cb["s_per_step"] * 1e3,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic", "impl": "reference",
                 "config": {"workload": DECODE_WORKLOAD, "M": 1, "layers": "qkv,o_proj,gate_up,down",
