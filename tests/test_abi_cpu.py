@@ -87,6 +87,8 @@ def test_noalloc_entry_point_limits(lib):
     assert f(ALIGNED, 1, 128, ALIGNED, ALIGNED, None, 48, 64, ALIGNED, None, 0) == -3     # group size
     assert f(MISALIGNED, 1, 128, ALIGNED, ALIGNED, None, 32, 64, ALIGNED, None, 0) == -4
     assert f(None, 0, 128, ALIGNED, ALIGNED, None, 32, 64, None, None, 0) == 0            # M == 0
+    # staged x (M x K) plus the partial slots must fit in the kernel's shared memory
+    assert f(ALIGNED, 8, 14336, ALIGNED, ALIGNED, None, 128, 4096, ALIGNED, None, 0) == -2
 
 
 def test_pack_validation(lib):
@@ -133,15 +135,15 @@ def test_debug_config_validation(lib):
     assert lib.w4a16_debug_set_config(2, arr, 5) == -9   # 256 KB partial tile does not fit
     assert lib.w4a16_debug_set_config(2, None, 0) == 0
     assert lib.w4a16_debug_set_config(9, None, 0) == -9
-    # per-warp-stream decode kernel: {mode} or {2, NBK, S, NW, NSW}
-    ok = (ctypes.c_int * 5)(2, 2, 4, 8, 2)
-    assert lib.w4a16_debug_set_config(5, ok, 5) == 0
-    for bad in ((2, 3, 1, 8, 2), (2, 2, 9, 8, 2), (2, 2, 1, 16, 2), (2, 2, 1, 8, 0), (3, 2, 1, 8, 2)):
-        arr = (ctypes.c_int * 5)(*bad)
-        assert lib.w4a16_debug_set_config(5, arr, 5) == -9, bad
-    assert lib.w4a16_debug_set_config(5, (ctypes.c_int * 1)(2), 1) == -9   # mode 2 needs a configuration
-    assert lib.w4a16_debug_set_config(5, (ctypes.c_int * 1)(0), 1) == 0
-    assert lib.w4a16_debug_set_config(5, None, 0) == 0
+    # decode kernel choice: {mode} or {mode, ring depth}
+    for good in ((0,), (1,), (2,), (2, 2), (2, 3), (2, 4), (0, 4)):
+        arr = (ctypes.c_int * len(good))(*good)
+        assert lib.w4a16_debug_set_config(6, arr, len(good)) == 0, good
+    for bad in ((3,), (-1,), (2, 1), (2, 5), (2, 3, 1)):
+        arr = (ctypes.c_int * len(bad))(*bad)
+        assert lib.w4a16_debug_set_config(6, arr, len(bad)) == -9, bad
+    assert lib.w4a16_debug_set_config(6, None, 0) == 0
+    assert lib.w4a16_debug_set_config(5, None, 0) == -9   # no such hook
 
 
 def test_binding_rejects_wrong_zero_point_dtype():

@@ -207,8 +207,9 @@ def w4a16_debug_set_config(which: int, vals=None) -> None:
     """Tuning hook (see include/w4a16.h): which=1 cluster decode kernel
     {R, NW, NB, NS, S}; which=2 prefill {BN, x stages, A stages, W stages[, KS]};
     which=3 programmatic dependent launch {flag}; which=4 balanced decode
-    kernel {on, ring depth}; which=5 per-warp-stream decode kernel {mode} or
-    {2, NBK, S, NW, NSW}.  vals=None restores the built-in choice."""
+    kernel {on, ring depth}; which=6 decode kernel choice {mode[, ring
+    depth]} (0 auto, 1 cluster kernel, 2 stream-K kernel).  vals=None
+    restores the built-in choice."""
     lib = load_library()
     if vals is None:
         rc = lib.w4a16_debug_set_config(which, None, 0)

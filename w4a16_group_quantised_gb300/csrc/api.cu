@@ -10,6 +10,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdlib>
 #include <cstring>
 #include <functional>
@@ -26,10 +27,24 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
+// Decode-kernel scratch of one stream: CTA partial slots and per-row-block
+// tickets (zero between calls).  Made by the first decode call on that
+// stream; calls on one stream run in order, so they never share it
+// concurrently.
+struct StreamScratch {
+    cudaStream_t stream;
+    float *ws;
+    int *cnt;
+};
+constexpr int kMaxStreamScratch = 64;
+
 struct DevState {
     std::once_flag once;
     int rc = W4A16_ERR_DEVICE;
     DeviceInfo info{};
+    std::mutex scratch_mu;
+    int n_scratch = 0;
+    StreamScratch scratch[kMaxStreamScratch];
 };
 DevState g_dev[kMaxDevices];
 
@@ -42,11 +57,36 @@ PrefillCfg g_prefill_cfg{};
 int g_pdl = 1;
 // balanced decode kernel: enabled flag and preferred ring depth
 int g_sk_on = 0, g_sk_ns = 4;
-// per-warp-stream decode kernel: 0 off (default: the cluster kernel measured faster on GB300),
-// 1 on (built-in configuration), 2 on (forced configuration)
-int g_warp_mode = 0;
-DecodeWarpCfg g_warp_cfg{2, 1, 8, 2};
-constexpr int kSkMaxRowBlocks = 1 << 16;   // N up to 1M rows
+// decode kernel choice: 0 = the built-in choice (the cluster kernel); 1 = the
+// cluster kernel; 2 = the stream-K kernel (error where it does not apply).
+// g_stream_d > 0 forces its ring depth.
+int g_decode_kernel = 0, g_stream_d = 0;
+// Streams whose last library launch wrote weights (w4a16_pack,
+// w4a16_pack_zeros): the next GEMM on such a stream is launched without
+// programmatic dependent launch, because the GEMM kernels read weights
+// before their grid-dependency wait.
+std::mutex g_pdl_mu;
+cudaStream_t g_pdl_unsafe[16];
+int g_n_pdl_unsafe = 0;
+
+void mark_weights_written(cudaStream_t s) {
+    std::lock_guard<std::mutex> lk(g_pdl_mu);
+    for (int i = 0; i < g_n_pdl_unsafe; ++i)
+        if (g_pdl_unsafe[i] == s) return;
+    if (g_n_pdl_unsafe < 16) g_pdl_unsafe[g_n_pdl_unsafe++] = s;
+    else g_pdl_unsafe[15] = s;
+}
+
+// true (and the mark cleared) if the last library launch on s wrote weights
+bool take_weights_written(cudaStream_t s) {
+    std::lock_guard<std::mutex> lk(g_pdl_mu);
+    for (int i = 0; i < g_n_pdl_unsafe; ++i)
+        if (g_pdl_unsafe[i] == s) {
+            g_pdl_unsafe[i] = g_pdl_unsafe[--g_n_pdl_unsafe];
+            return true;
+        }
+    return false;
+}
 
 void init_device(DevState &st, int dev) {
     DeviceInfo &d = st.info;
@@ -87,25 +127,12 @@ void init_device(DevState &st, int dev) {
         st.rc = W4A16_ERR_CUDA;
         return;
     }
-    // Workspace of the balanced decode kernel (allocated once per device,
-    // here, so that later calls never allocate).
-    {
-        const size_t wsf = decode_sk_workspace_floats(d.sm_count);
-        if (cudaMalloc(&d.sk_ws, wsf * sizeof(float)) != cudaSuccess ||
-            cudaMalloc(&d.sk_counters, sizeof(int) * kSkMaxRowBlocks) != cudaSuccess ||
-            cudaMemset(d.sk_counters, 0, sizeof(int) * kSkMaxRowBlocks) != cudaSuccess ||
-            cudaDeviceSynchronize() != cudaSuccess) {
-            st.rc = W4A16_ERR_CUDA;
-            return;
-        }
-        d.sk_max_rowblocks = kSkMaxRowBlocks;
-    }
     const char *e = std::getenv("W4A16_PDL");
     if (e && e[0] == '0') g_pdl = 0;
     st.rc = W4A16_OK;
 }
 
-int get_device(const DeviceInfo **out) {
+int get_device(const DeviceInfo **out, DevState **state = nullptr) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return W4A16_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return W4A16_ERR_DEVICE;
@@ -113,7 +140,48 @@ int get_device(const DeviceInfo **out) {
     std::call_once(st.once, init_device, std::ref(st), dev);
     if (st.rc != W4A16_OK) return st.rc;
     *out = &st.info;
+    if (state) *state = &st;
     return W4A16_OK;
+}
+
+// The decode scratch of stream s, made on the first decode call on s (one
+// cudaMalloc of the partial slots and one of the tickets, which are cleared
+// on s).  Returns false, allocating nothing, while s is being captured or
+// when the table is full; the caller then uses the cluster kernel, which
+// needs no scratch.
+bool stream_scratch(DevState &st, cudaStream_t s, float **ws, int **cnt) {
+    std::lock_guard<std::mutex> lk(st.scratch_mu);
+    for (int i = 0; i < st.n_scratch; ++i)
+        if (st.scratch[i].stream == s) {
+            *ws = st.scratch[i].ws;
+            *cnt = st.scratch[i].cnt;
+            return true;
+        }
+    if (st.n_scratch == kMaxStreamScratch) return false;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+        cudaGetLastError();
+        return false;
+    }
+    const size_t wsf = std::max(decode_stream_workspace_floats(st.info.sm_count),
+                                decode_sk_workspace_floats(st.info.sm_count));
+    float *w = nullptr;
+    int *c = nullptr;
+    if (cudaMalloc(&w, wsf * sizeof(float)) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (cudaMalloc(&c, sizeof(int) * kDecodeTickets) != cudaSuccess ||
+        cudaMemsetAsync(c, 0, sizeof(int) * kDecodeTickets, s) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(w);
+        if (c) cudaFree(c);
+        return false;
+    }
+    st.scratch[st.n_scratch++] = StreamScratch{s, w, c};
+    *ws = w;
+    *cnt = c;
+    return true;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -168,52 +236,51 @@ int run_gemm(const void *x, int M, int K, const int32_t *qw, const void *scales,
     if (path == W4A16_PATH_DECODE && M > W4A16_MAX_DECODE_M) return W4A16_ERR_SHAPE;
     if (M == 0) return W4A16_OK;
     const DeviceInfo *dev = nullptr;
-    rc = get_device(&dev);
+    DevState *st = nullptr;
+    rc = get_device(&dev, &st);
     if (rc != W4A16_OK) return rc;
     if (path == W4A16_PATH_AUTO) path = select_path_impl(M, N, K, G, qz == nullptr, dtype);
 
     GemmArgs a{x, qw, scales, qz, out, M, N, K, G, dtype};
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool asym = qz != nullptr;
+    bool pdl;
+    {
+        std::lock_guard<std::mutex> lk(g_cfg_mu);
+        pdl = g_pdl != 0;
+    }
+    if (take_weights_written(s)) pdl = false;
     cudaError_t e;
     if (path == W4A16_PATH_DECODE) {
-        int sk_on, ns_pref;
-        bool use_cluster_override;
+        int sk_on, ns_pref, kmode, dforce;
+        bool cluster_override;
+        DecodeCfg c;
         {
             std::lock_guard<std::mutex> lk(g_cfg_mu);
             sk_on = g_sk_on;
             ns_pref = g_sk_ns;
-            use_cluster_override = g_decode_override;
+            kmode = g_decode_kernel;
+            dforce = g_stream_d;
+            cluster_override = g_decode_override;
+            c = g_decode_cfg;
         }
-        if (!use_cluster_override && sk_on && (N + 15) / 16 <= dev->sk_max_rowblocks &&
-            decode_sk_applicable(M, K)) {
-            e = launch_decode_sk(a, ns_pref, *dev, dev->sk_ws, dev->sk_counters, s, g_pdl != 0);
+        if (cluster_override) kmode = 1;
+        float *ws = nullptr;
+        int *cnt = nullptr;
+        if (kmode != 1 && sk_on && (N + 15) / 16 <= kDecodeTickets && decode_sk_applicable(M, K) &&
+            stream_scratch(*st, s, &ws, &cnt)) {
+            e = launch_decode_sk(a, ns_pref, *dev, ws, cnt, s, pdl);
             return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
         }
-        int warp_mode;
-        DecodeWarpCfg wc;
-        {
-            std::lock_guard<std::mutex> lk(g_cfg_mu);
-            warp_mode = use_cluster_override ? 0 : g_warp_mode;
-            wc = g_warp_cfg;
+        if (kmode == 2 && decode_stream_applicable(M, N, K, G, asym) && stream_scratch(*st, s, &ws, &cnt)) {
+            e = launch_decode_stream(a, dforce, *dev, ws, cnt, s, pdl);
+            return e == cudaSuccess ? W4A16_OK : (e == cudaErrorInvalidValue ? W4A16_ERR_ARG : W4A16_ERR_CUDA);
         }
-        if (warp_mode != 0 && decode_warp_applicable(M, N, K)) {
-            if (warp_mode == 1)
-                wc = decode_warp_pick_cfg(M, N, K, G, qz == nullptr, dtype, dev->sm_count, dev->max_smem_optin);
-            else if (!decode_warp_cfg_valid(wc, M, N, K, G, qz != nullptr, dev->sm_count, dev->max_smem_optin))
-                return W4A16_ERR_ARG;
-            if (wc.NBK != 0) {
-                e = launch_decode_warp(a, wc, *dev, s, g_pdl != 0);
-                return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
-            }
-        }
-        DecodeCfg c;
-        {
-            std::lock_guard<std::mutex> lk(g_cfg_mu);
-            c = g_decode_override ? g_decode_cfg
-                                  : decode_pick_cfg(M, N, K, G, qz == nullptr, dtype, dev->sm_count, dev->smem_per_sm);
-        }
-        if (!decode_cfg_valid(c, M, K, G, qz != nullptr)) return W4A16_ERR_ARG;
-        e = launch_decode(a, c, *dev, s, g_pdl != 0);
+        if (kmode == 2) return W4A16_ERR_ARG;
+        if (!cluster_override)
+            c = decode_pick_cfg(M, N, K, G, qz == nullptr, dtype, dev->sm_count, dev->smem_per_sm);
+        if (!decode_cfg_valid(c, M, K, G, asym)) return W4A16_ERR_ARG;
+        e = launch_decode(a, c, *dev, s, pdl);
     } else {
         PrefillCfg c;
         {
@@ -221,7 +288,7 @@ int run_gemm(const void *x, int M, int K, const int32_t *qw, const void *scales,
             c = g_prefill_override ? g_prefill_cfg
                                    : prefill_pick_cfg(M, N, K, G, qz == nullptr, dtype, *dev);
         }
-        e = launch_prefill(a, c, *dev, s, g_pdl != 0);
+        e = launch_prefill(a, c, *dev, s, pdl);
     }
     return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
 }
@@ -234,6 +301,16 @@ int run_gemm(const void *x, int M, int K, const int32_t *qw, const void *scales,
 int validate_gemm_args(const void *x, int M, int K, const int32_t *qw, const void *scales, const int32_t *qz,
                        int G, int N, const void *out, int dtype) {
     return validate_gemm(x, M, K, qw, scales, qz, G, N, out, dtype);
+}
+
+bool pdl_enabled() {
+    std::lock_guard<std::mutex> lk(g_cfg_mu);
+    return g_pdl != 0;
+}
+
+bool pdl_for_stream(cudaStream_t s) {
+    const bool on = pdl_enabled();
+    return take_weights_written(s) ? false : on;
 }
 
 int *device_status_word() {
@@ -257,9 +334,9 @@ int w4a16_pack(const uint8_t *q, int N, int K, int32_t *qweight, w4a16_stream_t 
     const DeviceInfo *dev = nullptr;
     int rc = get_device(&dev);
     if (rc != W4A16_OK) return rc;
-    return launch_pack(q, N, K, qweight, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
-               ? W4A16_OK
-               : W4A16_ERR_CUDA;
+    if (launch_pack(q, N, K, qweight, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return W4A16_ERR_CUDA;
+    mark_weights_written(reinterpret_cast<cudaStream_t>(stream));
+    return W4A16_OK;
 }
 
 int w4a16_pack_zeros(const uint8_t *z, int N, int n_groups, int32_t *qzeros, w4a16_stream_t stream) {
@@ -271,10 +348,10 @@ int w4a16_pack_zeros(const uint8_t *z, int N, int n_groups, int32_t *qzeros, w4a
     const DeviceInfo *dev = nullptr;
     int rc = get_device(&dev);
     if (rc != W4A16_OK) return rc;
-    return launch_pack_zeros(z, N, n_groups, qzeros, reinterpret_cast<cudaStream_t>(stream)) ==
-                   cudaSuccess
-               ? W4A16_OK
-               : W4A16_ERR_CUDA;
+    if (launch_pack_zeros(z, N, n_groups, qzeros, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return W4A16_ERR_CUDA;
+    mark_weights_written(reinterpret_cast<cudaStream_t>(stream));
+    return W4A16_OK;
 }
 
 int w4a16_dequant_debug(const int32_t *qweight, const void *scales, const int32_t *qzeros_or_null,
@@ -353,10 +430,19 @@ int w4a16_last_device_error(void) {
 
 int w4a16_clear_device_error(void) {
     const DeviceInfo *dev = nullptr;
-    int rc = get_device(&dev);
+    DevState *st = nullptr;
+    int rc = get_device(&dev, &st);
     if (rc != W4A16_OK) return rc;
     int z = 0;
-    return cudaMemcpyToSymbol(g_w4a16_status, &z, sizeof(int)) == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return W4A16_ERR_CUDA;
+    // A kernel that gave up a wait may have left tickets counted: clear them.
+    {
+        std::lock_guard<std::mutex> lk(st->scratch_mu);
+        for (int i = 0; i < st->n_scratch; ++i)
+            if (cudaMemset(st->scratch[i].cnt, 0, sizeof(int) * kDecodeTickets) != cudaSuccess) return W4A16_ERR_CUDA;
+    }
+    if (cudaMemcpyToSymbol(g_w4a16_status, &z, sizeof(int)) != cudaSuccess) return W4A16_ERR_CUDA;
+    return cudaDeviceSynchronize() == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
 }
 
 int w4a16_version(void) { return 100; }
@@ -388,18 +474,14 @@ int w4a16_debug_set_config(int which, const int *vals, int n) {
         g_pdl = vals[0] != 0;
         return W4A16_OK;
     }
-    if (which == 5) {
-        if (n == 0) { g_warp_mode = 0; return W4A16_OK; }
-        if (vals == nullptr || (n != 1 && n != 5)) return W4A16_ERR_ARG;
-        if (vals[0] < 0 || vals[0] > 2 || (vals[0] == 2) != (n == 5)) return W4A16_ERR_ARG;
-        if (vals[0] == 2) {
-            const DecodeWarpCfg c{vals[1], vals[2], vals[3], vals[4]};
-            if (c.NBK != 1 && c.NBK != 2 && c.NBK != 4) return W4A16_ERR_ARG;
-            if (c.S < 1 || c.S > 8 || c.NSW < 1 || c.NSW > 8) return W4A16_ERR_ARG;
-            if (c.NW != 4 && c.NW != 8) return W4A16_ERR_ARG;
-            g_warp_cfg = c;
-        }
-        g_warp_mode = vals[0];
+    if (which == 6) {
+        if (n == 0) { g_decode_kernel = 0; g_stream_d = 0; return W4A16_OK; }
+        if (vals == nullptr || (n != 1 && n != 2)) return W4A16_ERR_ARG;
+        if (vals[0] < 0 || vals[0] > 2) return W4A16_ERR_ARG;
+        const int d = n == 2 ? vals[1] : 0;
+        if (d != 0 && (d < 2 || d > 4)) return W4A16_ERR_ARG;
+        g_decode_kernel = vals[0];
+        g_stream_d = d;
         return W4A16_OK;
     }
     if (which == 4) {

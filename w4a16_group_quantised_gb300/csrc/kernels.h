@@ -24,9 +24,6 @@ struct DeviceInfo {
     int smem_per_sm;        // shared memory of one SM (all resident CTAs together)
     int *status;            // device address of the status word
     void *encode_tiled;     // cuTensorMapEncodeTiled entry point
-    float *sk_ws;           // balanced decode kernel: partial sums
-    int *sk_counters;       // balanced decode kernel: per-row-block tickets (zero between calls)
-    int sk_max_rowblocks;   // capacity of sk_counters
     int prefill_clusters[9];  // prefill kernel: clusters of k CTAs resident at once (k = 1..8)
 };
 
@@ -50,19 +47,16 @@ size_t decode_smem_bytes(const DecodeCfg &c, int M, int K, int G, bool asym);
 cudaError_t launch_decode(const GemmArgs &a, const DecodeCfg &c, const DeviceInfo &dev,
                           cudaStream_t s, bool pdl);
 
-// ---- decode_warp.cu (one weight stream per warp; K a multiple of 128)
-struct DecodeWarpCfg {
-    int NBK;  // 128-k blocks per cell (1, 2, 4); a cell is 32 rows x NBK * 128 k
-    int S;    // CTAs along K in a cluster (1..8)
-    int NW;   // warps per CTA (4, 8)
-    int NSW;  // ring slots per warp (cells in flight)
-};
-bool decode_warp_applicable(int M, int N, int K);
-bool decode_warp_cfg_valid(const DecodeWarpCfg &c, int M, int N, int K, int G, bool asym, int sm_count,
-                           int smem_optin);
-DecodeWarpCfg decode_warp_pick_cfg(int M, int N, int K, int G, int sym, int dtype, int sm_count, int smem_optin);
-cudaError_t launch_decode_warp(const GemmArgs &a, const DecodeWarpCfg &c, const DeviceInfo &dev, cudaStream_t s,
-                               bool pdl);
+// ---- decode_stream.cu (stream-K kernel: K a multiple of 256, M <= 8)
+// Per-stream scratch: kDecodeTickets ints (zero between calls) and
+// decode_stream_workspace_floats(sm_count) floats of CTA partial slots.
+constexpr int kDecodeTickets = 1 << 16;
+bool decode_stream_applicable(int M, int N, int K, int G, bool asym);
+int decode_stream_pick_d(int M, int K, int G, bool asym);
+size_t decode_stream_smem_bytes(int M, int K, int G, bool asym, int D);
+size_t decode_stream_workspace_floats(int sm_count);
+cudaError_t launch_decode_stream(const GemmArgs &a, int D, const DeviceInfo &dev, float *ws, int *cnt,
+                                 cudaStream_t s, bool pdl);
 
 // ---- decode_sk.cu (balanced skinny kernel; needs a per-device workspace)
 size_t decode_sk_smem_bytes(int M, int K);
@@ -75,6 +69,10 @@ cudaError_t launch_decode_sk(const GemmArgs &a, int ns, const DeviceInfo &dev, f
 int validate_gemm_args(const void *x, int M, int K, const int32_t *qw, const void *scales, const int32_t *qz,
                        int G, int N, const void *out, int dtype);
 int *device_status_word();
+// Whether the next GEMM on s may use programmatic dependent launch: the
+// process-wide switch (W4A16_PDL, w4a16_debug_set_config(3)), and not right
+// after a library launch on s that wrote weights.  Clears that mark.
+bool pdl_for_stream(cudaStream_t s);
 
 // ---- prefill.cu
 struct PrefillCfg {

@@ -13,18 +13,24 @@
 // [16 rows][8 m] fp32 per CTA, one CTA per SM, up to kMaxSMs SMs) and one
 // ticket counter per 16-row block (up to kMaxRowBlocks, i.e. N <= 131072).
 // Larger problems or devices are rejected with W4A16_ERR_SHAPE /
-// W4A16_ERR_DEVICE.  Every device has its own copy of these arrays; the
-// first call on a device, with that device current, looks up their
-// addresses (cudaGetSymbolAddress) and clears the counters, so that first
-// call should come before any stream capture.  The kernel returns every
-// counter to zero itself.
+// W4A16_ERR_DEVICE, and so is a K whose staged x (M x K) and partial slots
+// do not fit in the kernel's shared memory (decode_sk_applicable, for
+// example M = 8 with K = 14336).  Every device has its own copy of these
+// arrays; the first call on a device, with that device current, looks up
+// their addresses (cudaGetSymbolAddress) and clears the counters, so that
+// first call should come before any stream capture: made during a capture
+// it returns W4A16_ERR_DEVICE without touching the device, and a later call
+// outside the capture sets up as usual.  A set-up that fails is retried by
+// the next call.  The kernel returns every counter to zero itself.
+//
+// Programmatic dependent launch follows the library's switch (W4A16_PDL,
+// w4a16_debug_set_config(3)) as w4a16_gemm does.
 //
 // All calls on one device share the scratch: calls whose kernels overlap on
 // the GPU (for instance on two streams without an ordering between them)
 // race on it and give wrong results.  Calls issued in order on one stream
 // are safe (the kernel touches the scratch only after its grid-dependency
 // wait).
-#include <functional>
 #include <mutex>
 
 #include "kernels.h"
@@ -42,7 +48,8 @@ static __device__ __align__(256) int g_noalloc_counters[kMaxRowBlocks];         
 
 constexpr int kMaxDevices = 64;
 struct NoAllocState {
-    std::once_flag once;
+    std::mutex mu;
+    bool ready = false;
     int rc = W4A16_ERR_DEVICE;
     DeviceInfo info{};
     float *ws = nullptr;
@@ -50,6 +57,7 @@ struct NoAllocState {
 };
 NoAllocState g_state[kMaxDevices];
 
+// Sets st.rc; st.ready only on success (a failed set-up is retried by the next call).
 void set_up(NoAllocState &st, int dev) {
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
@@ -79,6 +87,7 @@ void set_up(NoAllocState &st, int dev) {
     st.ws = static_cast<float *>(ws);
     st.counters = static_cast<int *>(counters);
     st.rc = W4A16_OK;
+    st.ready = true;
 }
 
 }  // namespace
@@ -97,10 +106,19 @@ extern "C" int w4a16_gemm_decode_noalloc(const void *x, int M, int K, const int3
     if (cudaGetDevice(&dev) != cudaSuccess) return W4A16_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return W4A16_ERR_DEVICE;
     NoAllocState &st = g_state[dev];
-    std::call_once(st.once, set_up, std::ref(st), dev);
-    if (st.rc != W4A16_OK) return st.rc;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    {
+        std::lock_guard<std::mutex> lk(st.mu);
+        if (!st.ready) {
+            // set-up synchronises the device: never during a capture
+            cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+            if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return W4A16_ERR_CUDA;
+            if (cs != cudaStreamCaptureStatusNone) return W4A16_ERR_DEVICE;
+            set_up(st, dev);
+            if (!st.ready) return st.rc;
+        }
+    }
     GemmArgs a{x, qweight, scales, qzeros_or_null, out, M, N, K, G, (int)dtype};
-    const cudaError_t e = launch_decode_sk(a, 4, st.info, st.ws, st.counters,
-                                           reinterpret_cast<cudaStream_t>(stream), true);
+    const cudaError_t e = launch_decode_sk(a, 4, st.info, st.ws, st.counters, s, pdl_for_stream(s));
     return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
 }
