@@ -32,6 +32,17 @@
  * the tensor-map encoder) is set up on the first call on each device; make
  * that first call outside stream capture.
  *
+ * Programmatic dependent launch: the GEMM kernels are launched so that they
+ * may start while the kernel before them on the stream is still running,
+ * and they read qweight, scales and qzeros before waiting for it (x, out
+ * only after).  So the kernel immediately before a GEMM on its stream must
+ * not write that GEMM's weights, scales or zero points.  The library's own
+ * w4a16_pack / w4a16_pack_zeros are handled: the next GEMM on the same
+ * stream is launched without early start.  Anything else that writes
+ * weights (a copy, a user kernel) needs some other work or an event between
+ * it and the GEMM, or early start switched off (environment W4A16_PDL=0 or
+ * w4a16_debug_set_config(3, {0}, 1)).
+ *
  * Errors: arguments are validated on the host before anything is launched;
  * an invalid call returns a negative w4a16_status_t and launches nothing.
  * M == 0 (or N == 0 for pack) is a valid no-op.  A launch failure returns
@@ -72,11 +83,12 @@ typedef enum {
     W4A16_ERR_ARG = -9       /* other invalid argument (e.g. path enum)       */
 } w4a16_status_t;
 
-/* Concurrency: the skinny decode kernel keeps per-row-block tickets and
- * partial sums in a workspace owned by the library (one per device, made by
- * the first call on that device).  Decode-path calls on one device must
- * therefore not run concurrently on different streams; calls on one stream
- * (the usual case, with or without CUDA graphs) are always safe. */
+/* Concurrency: the default kernels keep no state between calls, so calls on
+ * any streams may overlap.  The balanced decode kernel (an option, see
+ * w4a16_debug_set_config which = 4) keeps per-row-block tickets and partial
+ * sums in a scratch buffer per stream, made by the first call on that stream
+ * with the option on (outside stream capture; during a capture the call
+ * falls back to the default decode kernel instead of allocating). */
 
 /* Limits checked by the validation (shapes must also fit in int32 indexing). */
 #define W4A16_MAX_DECODE_M 8
@@ -95,14 +107,31 @@ int w4a16_pack_zeros(const uint8_t *z, int N, int n_groups, int32_t *qzeros,
                      w4a16_stream_t stream);
 
 /* Materialise the dequantised weights: out[n, k] = RN_dtype((q - z) * s),
- * device [N, K] of dtype.  Bit-exact with the definition above.  Uses the same
- * device dequantisation routines as the GEMM kernels.  Validation as for
- * w4a16_gemm (G, K % G, N % 8, alignment).
+ * device [N, K] of dtype, k in natural order.  Bit-exact with the definition
+ * above.  Runs the register routine of the prefill GEMM kernel (the same
+ * code path as w4a16_dequant_debug_ex with W4A16_DQ_PREFILL).  Validation as
+ * for w4a16_gemm (G, K % G, N % 8, alignment).
  * Source: "[ROCm][Kernel] Add HybridW4A16LinearKernel", PR description
  * (symmetric bias 8 / per-group zero points; the magic-number dequant). */
 int w4a16_dequant_debug(const int32_t *qweight, const void *scales,
                         const int32_t *qzeros_or_null, int G, int N, int K, void *out,
                         w4a16_dtype_t dtype, w4a16_stream_t stream);
+
+/* Which GEMM kernel's dequantisation routine w4a16_dequant_debug_ex runs. */
+typedef enum {
+    W4A16_DQ_PREFILL = 0,    /* natural (k, k+1) pairs, constants as kernel data       */
+    W4A16_DQ_DECODE = 1,     /* (k, k+4) pairs, constants as kernel data (cluster decode) */
+    W4A16_DQ_BALANCED = 2    /* (k, k+4) pairs, immediate constants (balanced decode)  */
+} w4a16_dq_routine_t;
+
+/* w4a16_dequant_debug with the routine chosen: each GEMM kernel's own
+ * dequantisation code, its output put in natural k order, so that a test can
+ * hold every routine to the definition bit for bit.  routine outside the enum
+ * -> W4A16_ERR_ARG; otherwise as w4a16_dequant_debug.
+ * Source: as w4a16_dequant_debug. */
+int w4a16_dequant_debug_ex(const int32_t *qweight, const void *scales,
+                           const int32_t *qzeros_or_null, int G, int N, int K, void *out,
+                           w4a16_dtype_t dtype, w4a16_stream_t stream, int routine);
 
 /* y = x . dequant(W)^T on `stream`.  x, scales and out share `dtype`.
  * Requires M >= 0, N > 0 with N % 8 == 0, K > 0 with K % G == 0,
@@ -151,12 +180,17 @@ int w4a16_select_path(int M, int N, int K, int G, int sym, int dtype);
  * host-side validation are those of w4a16_gemm; the result is that of the
  * balanced decode kernel (debug configuration which = 4).  The kernel's
  * scratch is static device memory of fixed size, so: M must be 0..8 and N at
- * most 131072 (W4A16_ERR_SHAPE otherwise), and the device may have at most
- * 256 SMs (W4A16_ERR_DEVICE).  The first call on a device, with that device
- * current, sets the scratch up (looks up its address and clears it); make
- * that first call before any stream capture.  All calls on a device share
- * the scratch: calls whose kernels overlap on the GPU race on it; calls in
- * order on one stream are safe. */
+ * most 131072, and the staged x (M x K values) plus the kernel's partial
+ * slots must fit in its 220 KB of shared memory (for example M = 8 with
+ * K = 14336 does not) -- W4A16_ERR_SHAPE otherwise; the device may have at
+ * most 256 SMs (W4A16_ERR_DEVICE).  The first call on a device, with that
+ * device current, sets the scratch up (looks up its address and clears it);
+ * make that first call before any stream capture: made during a capture it
+ * returns W4A16_ERR_DEVICE and touches nothing, and the next call outside a
+ * capture sets up as usual (a failed set-up is retried).  Programmatic
+ * dependent launch follows the same switch as w4a16_gemm.  All calls on a
+ * device share the scratch: calls whose kernels overlap on the GPU race on
+ * it; calls in order on one stream are safe. */
 int w4a16_gemm_decode_noalloc(const void *x, int M, int K, const int32_t *qweight,
                               const void *scales, const int32_t *qzeros_or_null, int G, int N,
                               void *out, w4a16_stream_t stream, w4a16_dtype_t dtype);
@@ -183,12 +217,7 @@ int w4a16_version(void);
  * which = 3: programmatic dependent launch on/off, vals = {flag}, n = 1;
  * which = 4: balanced decode kernel vals = {on (1) / off (0), load ring
  * depth in units (2, 4 or 6)}, n = 2;
- * which = 5: per-warp-stream decode kernel (for K % 128 == 0; off by
- * default), vals = {0} off, {1} on with the built-in configuration (n = 1),
- * or {2, NBK, S, NW, NSW} on with a forced configuration (128-k blocks per
- * cell in {1, 2, 4}, cluster CTAs along K in 1..8, warps per CTA in {4, 8},
- * ring slots per warp in 1..8), n = 5; n = 0 restores {0}.
- * n = 0 restores the built-in choice for which = 1, 2, 4 or 5.  An invalid
+ * n = 0 restores the built-in choice for which = 1, 2 or 4.  An invalid
  * configuration is rejected here or, for the decode shape limits, by the
  * next w4a16_gemm call with W4A16_ERR_ARG. */
 int w4a16_debug_set_config(int which, const int *vals, int n);

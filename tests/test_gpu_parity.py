@@ -36,43 +36,61 @@ def run_case(w, p, path, rows=None):
 
 
 # ------------------------------------------------------------------ packing / dequant
+ROUTINES = [0, 1, 2]          # prefill, decode (runtime constants), balanced decode
+ROUTINE_IDS = ["prefill", "decode", "balanced"]
+
+
+@pytest.mark.parametrize("routine", ROUTINES, ids=ROUTINE_IDS)
 @pytest.mark.parametrize("dtype", [0, 1])
 @pytest.mark.parametrize("sym", [True, False])
 @pytest.mark.parametrize("G", [32, 64, 128])
-def test_dequant_bit_exact(cuda_lib, dtype, sym, G):
+def test_dequant_bit_exact(cuda_lib, dtype, sym, G, routine):
+    """Each GEMM kernel's own dequantiser, run over a whole matrix and written
+    in natural order, equals the oracle's RN((q - z) * s) bit for bit."""
     w = cuda_lib
     p = make_problem(1, 264, 1152, G, sym, dtype, seed=100 + G)
     d = to_device(p, w)
-    got = tensor_to_bits(w.w4a16_dequant_debug(d["qweight"], d["scales"], d["qzeros"], G))
+    got = tensor_to_bits(w.w4a16_dequant_debug(d["qweight"], d["scales"], d["qzeros"], G,
+                                               routine=routine))
     ref = oracle.dequant(d["ref_qw"], p.scales, d["ref_qz"], G, p.N, p.K, dtype)
     assert np.array_equal(got, ref)
 
 
-@pytest.mark.parametrize("dtype", [0, 1])
-def test_dequant_exhaustive_scales(cuda_lib, dtype):
-    """Every finite 16-bit scale pattern times every q - z in [-15, 15]:
-    bit-exact against the oracle's RN_dtype((q - z) * s).  Row n uses scale
-    pattern n; group 0 has z = 15 (q - z = -15..0), group 1 z = 0 (0..15)."""
-    w = cuda_lib
+def exhaustive_case(dtype):
+    """Row n holds scale bit pattern n (non-finite patterns replaced by 0);
+    group 0 has z = 15 (q - z = -15..0), group 1 z = 0 (q - z = 0..15), and
+    each group runs q over 0..15 twice."""
     N, K, G = 65536, 64, 32
     pat = np.arange(65536, dtype=np.uint16)
     vals = oracle.bits_to_float64(pat, dtype)
     s_bits = np.where(np.isfinite(vals), pat, 0).astype(np.uint16)
     scales = np.repeat(s_bits[:, None], 2, axis=1)
-    q = np.tile(np.concatenate([np.arange(16), np.arange(16), np.arange(16), np.arange(16)])
-                .astype(np.uint8), (N, 1))
+    q = np.tile(np.concatenate([np.arange(16)] * 4).astype(np.uint8), (N, 1))
     z = np.tile(np.array([15, 0], dtype=np.uint8), (N, 1))
     qw = oracle.pack(q)
     qz = oracle.pack_zeros(z)
+    ref = oracle.dequant(qw, scales, qz, G, N, K, dtype)
+    return N, K, G, qw, qz, scales, s_bits, ref
+
+
+@pytest.mark.parametrize("routine", ROUTINES, ids=ROUTINE_IDS)
+@pytest.mark.parametrize("dtype", [0, 1])
+def test_dequant_exhaustive_scales(cuda_lib, dtype, routine):
+    """Every finite 16-bit scale pattern (normal, subnormal, zero, negative)
+    times every q - z in [-15, 15], through each GEMM kernel's dequantiser:
+    bit-exact against the oracle's RN_dtype((q - z) * s)."""
+    w = cuda_lib
+    N, K, G, qw, qz, scales, s_bits, ref = exhaustive_case(dtype)
     got = tensor_to_bits(w.w4a16_dequant_debug(torch.from_numpy(qw).cuda(),
                                                bits_to_tensor(scales, dtype),
-                                               torch.from_numpy(qz).cuda(), G))
-    ref = oracle.dequant(qw, scales, qz, G, N, K, dtype)
+                                               torch.from_numpy(qz).cuda(), G,
+                                               routine=routine))
     sv = np.abs(oracle.bits_to_float64(s_bits, dtype))
     min_normal = 2.0 ** -14 if dtype == 0 else 2.0 ** -126
-    normal_rows = (sv >= min_normal) | (sv == 0)
+    subnormal = (sv < min_normal) & (sv > 0)
     mism = (got != ref).any(axis=1)
-    assert not mism[normal_rows].any(), f"{mism[normal_rows].sum()} rows with normal scales differ"
+    assert not mism[~subnormal].any(), f"{mism[~subnormal].sum()} rows with normal scales differ"
+    assert not mism[subnormal].any(), f"{mism[subnormal].sum()} rows with subnormal scales differ"
 
 
 def test_pack_edge_values(cuda_lib):

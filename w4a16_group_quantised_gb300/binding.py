@@ -52,6 +52,7 @@ def load_library():
             "w4a16_pack": [P, I, I, P, P],
             "w4a16_pack_zeros": [P, I, I, P, P],
             "w4a16_dequant_debug": [P, P, P, I, I, I, P, I, P],
+            "w4a16_dequant_debug_ex": [P, P, P, I, I, I, P, I, P, I],
             "w4a16_gemm": [P, I, I, P, P, P, I, I, P, P, I],
             "w4a16_gemm_f16": [P, I, I, P, P, P, I, I, P, P],
             "w4a16_gemm_bf16": [P, I, I, P, P, P, I, I, P, P],
@@ -125,8 +126,12 @@ def w4a16_pack_zeros(z, qzeros=None, stream=None):
     return qzeros
 
 
-def w4a16_dequant_debug(qweight, scales, qzeros, G: int, out=None, stream=None):
-    """Materialise RN_dtype((q - z) * s) as a [N, K] tensor of the scales' dtype."""
+DQ_PREFILL, DQ_DECODE, DQ_BALANCED = 0, 1, 2
+
+
+def w4a16_dequant_debug(qweight, scales, qzeros, G: int, out=None, stream=None, routine=None):
+    """Materialise RN_dtype((q - z) * s) as a [N, K] tensor of the scales' dtype
+    (routine: None = w4a16_dequant_debug, else the w4a16_dequant_debug_ex routine)."""
     import torch
     _require_int32("qweight", qweight)
     _require_int32("qzeros", qzeros)
@@ -136,9 +141,13 @@ def w4a16_dequant_debug(qweight, scales, qzeros, G: int, out=None, stream=None):
     if out is None:
         out = torch.empty((N, K), dtype=scales.dtype, device=qweight.device)
     lib = load_library()
-    _check("w4a16_dequant_debug",
-           lib.w4a16_dequant_debug(_p(qweight), _p(scales), _p(qzeros), G, N, K, _p(out), dt,
-                                   _stream_ptr(stream)))
+    if routine is None:
+        rc = lib.w4a16_dequant_debug(_p(qweight), _p(scales), _p(qzeros), G, N, K, _p(out), dt,
+                                     _stream_ptr(stream))
+    else:
+        rc = lib.w4a16_dequant_debug_ex(_p(qweight), _p(scales), _p(qzeros), G, N, K, _p(out), dt,
+                                        _stream_ptr(stream), routine)
+    _check("w4a16_dequant_debug", rc)
     return out
 
 
@@ -207,9 +216,7 @@ def w4a16_debug_set_config(which: int, vals=None) -> None:
     """Tuning hook (see include/w4a16.h): which=1 cluster decode kernel
     {R, NW, NB, NS, S}; which=2 prefill {BN, x stages, A stages, W stages[, KS]};
     which=3 programmatic dependent launch {flag}; which=4 balanced decode
-    kernel {on, ring depth}; which=6 decode kernel choice {mode[, ring
-    depth]} (0 auto, 1 cluster kernel, 2 stream-K kernel).  vals=None
-    restores the built-in choice."""
+    kernel {on, ring depth}.  vals=None restores the built-in choice."""
     lib = load_library()
     if vals is None:
         rc = lib.w4a16_debug_set_config(which, None, 0)

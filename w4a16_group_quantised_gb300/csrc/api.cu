@@ -27,10 +27,9 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
-// Decode-kernel scratch of one stream: CTA partial slots and per-row-block
-// tickets (zero between calls).  Made by the first decode call on that
-// stream; calls on one stream run in order, so they never share it
-// concurrently.
+// Balanced-decode-kernel scratch of one stream: CTA partial slots and
+// per-row-block tickets (zero between calls).  Calls on one stream run in
+// order, so they never share it concurrently.
 struct StreamScratch {
     cudaStream_t stream;
     float *ws;
@@ -57,10 +56,6 @@ PrefillCfg g_prefill_cfg{};
 int g_pdl = 1;
 // balanced decode kernel: enabled flag and preferred ring depth
 int g_sk_on = 0, g_sk_ns = 4;
-// decode kernel choice: 0 = the built-in choice (the cluster kernel); 1 = the
-// cluster kernel; 2 = the stream-K kernel (error where it does not apply).
-// g_stream_d > 0 forces its ring depth.
-int g_decode_kernel = 0, g_stream_d = 0;
 // Streams whose last library launch wrote weights (w4a16_pack,
 // w4a16_pack_zeros): the next GEMM on such a stream is launched without
 // programmatic dependent launch, because the GEMM kernels read weights
@@ -144,11 +139,12 @@ int get_device(const DeviceInfo **out, DevState **state = nullptr) {
     return W4A16_OK;
 }
 
-// The decode scratch of stream s, made on the first decode call on s (one
-// cudaMalloc of the partial slots and one of the tickets, which are cleared
-// on s).  Returns false, allocating nothing, while s is being captured or
-// when the table is full; the caller then uses the cluster kernel, which
-// needs no scratch.
+// The balanced decode kernel's scratch for stream s, made on the first call
+// that enables that kernel on s (one cudaMalloc of the partial slots and one
+// of the tickets, which are cleared on s).  Returns false, allocating
+// nothing, while s is being captured or when the table is full; the caller
+// then uses the cluster kernel, which needs no scratch.  The default path
+// never gets here, so a default w4a16_gemm call never allocates.
 bool stream_scratch(DevState &st, cudaStream_t s, float **ws, int **cnt) {
     std::lock_guard<std::mutex> lk(st.scratch_mu);
     for (int i = 0; i < st.n_scratch; ++i)
@@ -163,8 +159,7 @@ bool stream_scratch(DevState &st, cudaStream_t s, float **ws, int **cnt) {
         cudaGetLastError();
         return false;
     }
-    const size_t wsf = std::max(decode_stream_workspace_floats(st.info.sm_count),
-                                decode_sk_workspace_floats(st.info.sm_count));
+    const size_t wsf = decode_sk_workspace_floats(st.info.sm_count);
     float *w = nullptr;
     int *c = nullptr;
     if (cudaMalloc(&w, wsf * sizeof(float)) != cudaSuccess) {
@@ -252,31 +247,23 @@ int run_gemm(const void *x, int M, int K, const int32_t *qw, const void *scales,
     if (take_weights_written(s)) pdl = false;
     cudaError_t e;
     if (path == W4A16_PATH_DECODE) {
-        int sk_on, ns_pref, kmode, dforce;
+        int sk_on, ns_pref;
         bool cluster_override;
         DecodeCfg c;
         {
             std::lock_guard<std::mutex> lk(g_cfg_mu);
-            sk_on = g_sk_on;
+            sk_on = g_sk_on && !g_decode_override;
             ns_pref = g_sk_ns;
-            kmode = g_decode_kernel;
-            dforce = g_stream_d;
             cluster_override = g_decode_override;
             c = g_decode_cfg;
         }
-        if (cluster_override) kmode = 1;
         float *ws = nullptr;
         int *cnt = nullptr;
-        if (kmode != 1 && sk_on && (N + 15) / 16 <= kDecodeTickets && decode_sk_applicable(M, K) &&
+        if (sk_on && (N + 15) / 16 <= kDecodeTickets && decode_sk_applicable(M, K) &&
             stream_scratch(*st, s, &ws, &cnt)) {
             e = launch_decode_sk(a, ns_pref, *dev, ws, cnt, s, pdl);
             return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
         }
-        if (kmode == 2 && decode_stream_applicable(M, N, K, G, asym) && stream_scratch(*st, s, &ws, &cnt)) {
-            e = launch_decode_stream(a, dforce, *dev, ws, cnt, s, pdl);
-            return e == cudaSuccess ? W4A16_OK : (e == cudaErrorInvalidValue ? W4A16_ERR_ARG : W4A16_ERR_CUDA);
-        }
-        if (kmode == 2) return W4A16_ERR_ARG;
         if (!cluster_override)
             c = decode_pick_cfg(M, N, K, G, qz == nullptr, dtype, dev->sm_count, dev->smem_per_sm);
         if (!decode_cfg_valid(c, M, K, G, asym)) return W4A16_ERR_ARG;
@@ -354,8 +341,9 @@ int w4a16_pack_zeros(const uint8_t *z, int N, int n_groups, int32_t *qzeros, w4a
     return W4A16_OK;
 }
 
-int w4a16_dequant_debug(const int32_t *qweight, const void *scales, const int32_t *qzeros_or_null,
-                        int G, int N, int K, void *out, w4a16_dtype_t dtype, w4a16_stream_t stream) {
+int w4a16_dequant_debug_ex(const int32_t *qweight, const void *scales, const int32_t *qzeros_or_null, int G,
+                           int N, int K, void *out, w4a16_dtype_t dtype, w4a16_stream_t stream, int routine) {
+    if (routine < W4A16_DQ_PREFILL || routine > W4A16_DQ_BALANCED) return W4A16_ERR_ARG;
     int rc = validate_common(0, N, K, G, (int)dtype);
     if (rc != W4A16_OK) return rc;
     if (qweight == nullptr || scales == nullptr || out == nullptr) return W4A16_ERR_NULL;
@@ -364,10 +352,15 @@ int w4a16_dequant_debug(const int32_t *qweight, const void *scales, const int32_
     const DeviceInfo *dev = nullptr;
     rc = get_device(&dev);
     if (rc != W4A16_OK) return rc;
-    return launch_dequant(qweight, scales, qzeros_or_null, G, N, K, out, (int)dtype,
+    return launch_dequant(qweight, scales, qzeros_or_null, G, N, K, out, (int)dtype, routine,
                           reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? W4A16_OK
                : W4A16_ERR_CUDA;
+}
+
+int w4a16_dequant_debug(const int32_t *qweight, const void *scales, const int32_t *qzeros_or_null,
+                        int G, int N, int K, void *out, w4a16_dtype_t dtype, w4a16_stream_t stream) {
+    return w4a16_dequant_debug_ex(qweight, scales, qzeros_or_null, G, N, K, out, dtype, stream, W4A16_DQ_PREFILL);
 }
 
 int w4a16_gemm(const void *x, int M, int K, const int32_t *qweight, const void *scales,
@@ -472,16 +465,6 @@ int w4a16_debug_set_config(int which, const int *vals, int n) {
     if (which == 3) {
         if (n != 1 || vals == nullptr) return W4A16_ERR_ARG;
         g_pdl = vals[0] != 0;
-        return W4A16_OK;
-    }
-    if (which == 6) {
-        if (n == 0) { g_decode_kernel = 0; g_stream_d = 0; return W4A16_OK; }
-        if (vals == nullptr || (n != 1 && n != 2)) return W4A16_ERR_ARG;
-        if (vals[0] < 0 || vals[0] > 2) return W4A16_ERR_ARG;
-        const int d = n == 2 ? vals[1] : 0;
-        if (d != 0 && (d < 2 || d > 4)) return W4A16_ERR_ARG;
-        g_decode_kernel = vals[0];
-        g_stream_d = d;
         return W4A16_OK;
     }
     if (which == 4) {

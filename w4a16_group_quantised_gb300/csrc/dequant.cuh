@@ -197,6 +197,13 @@ __device__ __forceinline__ void dq_word_i4(uint32_t w, uint32_t zl2, uint32_t zh
     o[3] = hmul2_u<DT>(hsub2_u<DT>(v3, zh2), s2);
 }
 
+// zhi2 from zlo2: the same zero point moved from the low-magic to the
+// high-magic position in both lanes (as the decode kernels derive it).
+template <int DT>
+__device__ __forceinline__ uint32_t zhi_from_zlo_dq(uint32_t zl2) {
+    return ((zl2 & 0x000F000Fu) << (DT == 0 ? 4 : 3)) | rep2(Dtype<DT>::kMagicHi);
+}
+
 // Zero point of row n, group g: nibble n%8 of qzeros[n/8, g]; 8 when symmetric.
 __device__ __forceinline__ uint32_t zero_point(const int32_t *qz, int n, int g, int ng) {
     if (qz == nullptr) return 8u;

@@ -31,7 +31,7 @@ struct DeviceInfo {
 cudaError_t launch_pack(const uint8_t *q, int N, int K, int32_t *qweight, cudaStream_t s);
 cudaError_t launch_pack_zeros(const uint8_t *z, int N, int ng, int32_t *qzeros, cudaStream_t s);
 cudaError_t launch_dequant(const int32_t *qweight, const void *scales, const int32_t *qzeros,
-                           int G, int N, int K, void *out, int dtype, cudaStream_t s);
+                           int G, int N, int K, void *out, int dtype, int routine, cudaStream_t s);
 
 // ---- decode.cu
 struct DecodeCfg {
@@ -47,16 +47,9 @@ size_t decode_smem_bytes(const DecodeCfg &c, int M, int K, int G, bool asym);
 cudaError_t launch_decode(const GemmArgs &a, const DecodeCfg &c, const DeviceInfo &dev,
                           cudaStream_t s, bool pdl);
 
-// ---- decode_stream.cu (stream-K kernel: K a multiple of 256, M <= 8)
-// Per-stream scratch: kDecodeTickets ints (zero between calls) and
-// decode_stream_workspace_floats(sm_count) floats of CTA partial slots.
+// Per-stream scratch of the balanced decode kernel: kDecodeTickets ints
+// (zero between calls) and decode_sk_workspace_floats(sm_count) floats.
 constexpr int kDecodeTickets = 1 << 16;
-bool decode_stream_applicable(int M, int N, int K, int G, bool asym);
-int decode_stream_pick_d(int M, int K, int G, bool asym);
-size_t decode_stream_smem_bytes(int M, int K, int G, bool asym, int D);
-size_t decode_stream_workspace_floats(int sm_count);
-cudaError_t launch_decode_stream(const GemmArgs &a, int D, const DeviceInfo &dev, float *ws, int *cnt,
-                                 cudaStream_t s, bool pdl);
 
 // ---- decode_sk.cu (balanced skinny kernel; needs a per-device workspace)
 size_t decode_sk_smem_bytes(int M, int K);

@@ -1,6 +1,6 @@
 // pack.cu -- packing of 4-bit weights and zero points, and the debug
-// dequantisation kernel (materialises RN_dtype((q - z) * s) with the same
-// register routines the GEMM kernels use).
+// dequantisation kernel (materialises RN_dtype((q - z) * s) with the
+// register routine of a chosen GEMM kernel).
 //
 // Formats: "[ROCm][Kernel] Add HybridW4A16LinearKernel: Triton prefill + HIP
 // skinny decode", PR description (weights [N, K//8], 8 per int32 along K);
@@ -43,10 +43,18 @@ __global__ void pack_zeros_kernel(const uint8_t *__restrict__ z, int rows8, int 
     }
 }
 
-// One thread per weight word: 8 outputs (16 bytes) of row n.
-template <int DT>
+// One thread per weight word: 8 outputs (16 bytes) of row n, in natural k
+// order, computed by the dequantisation routine a GEMM kernel uses:
+//   ROUTINE 0: dq_word_seq_rt with the prefill kernel's constants;
+//   ROUTINE 1: dq_word_i4_rt with the cluster decode kernel's constants and
+//              its zero-point words (zlo2, and zhi_from_zlo for asymmetric
+//              weights / zhi2(8) for symmetric ones), the (k, k+4) pairs put
+//              back in natural order;
+//   ROUTINE 2: dq_word_i4 (immediate constants), as the balanced decode
+//              kernel runs it.
+template <int DT, int ROUTINE>
 __global__ void dequant_kernel(const int32_t *__restrict__ qw, const uint16_t *__restrict__ scales,
-                               const int32_t *__restrict__ qz, int G, int N, int K,
+                               const int32_t *__restrict__ qz, int G, int N, int K, DqConsts dc,
                                uint4 *__restrict__ out) {
     const int K8 = K >> 3, ng = K / G;
     long long total = (long long)N * K8;
@@ -57,8 +65,21 @@ __global__ void dequant_kernel(const int32_t *__restrict__ qw, const uint16_t *_
         uint32_t z = zero_point(qz, n, g, ng);
         uint32_t s = scales[(size_t)n * ng + g];
         uint32_t o[4];
-        dq_word_seq<DT>((uint32_t)qw[i], zseq2<DT>(z), rep2(s), o);
-        out[i] = make_uint4(o[0], o[1], o[2], o[3]);
+        const uint32_t w = (uint32_t)qw[i];
+        if (ROUTINE == 0) {
+            dq_word_seq_rt<DT>(w, dc, zseq2<DT>(z), rep2(s), o);
+            out[i] = make_uint4(o[0], o[1], o[2], o[3]);
+        } else {
+            const uint32_t zl = zlo2<DT>(z);
+            const uint32_t zh = qz != nullptr ? zhi_from_zlo_dq<DT>(zl) : zhi2<DT>(8u);
+            if (ROUTINE == 1)
+                dq_word_i4_rt<DT>(w, dc, zl, zh, rep2(s), o);
+            else
+                dq_word_i4<DT>(w, zl, zh, rep2(s), o);
+            // o = (w0, w4), (w1, w5), (w2, w6), (w3, w7) -> natural order
+            out[i] = make_uint4(__byte_perm(o[0], o[1], 0x5410), __byte_perm(o[2], o[3], 0x5410),
+                                __byte_perm(o[0], o[1], 0x7632), __byte_perm(o[2], o[3], 0x7632));
+        }
     }
 }
 
@@ -83,17 +104,26 @@ cudaError_t launch_pack_zeros(const uint8_t *z, int N, int ng, int32_t *qzeros, 
     return cudaGetLastError();
 }
 
+template <int DT>
+static void launch_dequant_t(int routine, int grid, cudaStream_t s, const int32_t *qweight, const uint16_t *scales,
+                             const int32_t *qzeros, int G, int N, int K, uint4 *out) {
+    if (routine == 0)
+        dequant_kernel<DT, 0><<<grid, 256, 0, s>>>(qweight, scales, qzeros, G, N, K, dq_consts_seq(DT), out);
+    else if (routine == 1)
+        dequant_kernel<DT, 1><<<grid, 256, 0, s>>>(qweight, scales, qzeros, G, N, K, dq_consts_i4(DT), out);
+    else
+        dequant_kernel<DT, 2><<<grid, 256, 0, s>>>(qweight, scales, qzeros, G, N, K, dq_consts_i4(DT), out);
+}
+
 cudaError_t launch_dequant(const int32_t *qweight, const void *scales, const int32_t *qzeros,
-                           int G, int N, int K, void *out, int dtype, cudaStream_t s) {
+                           int G, int N, int K, void *out, int dtype, int routine, cudaStream_t s) {
     long long words = (long long)N * (K / 8);
     if (words == 0) return cudaSuccess;
     int grid = grid_for(words, 256);
     if (dtype == 0)
-        dequant_kernel<0><<<grid, 256, 0, s>>>(qweight, (const uint16_t *)scales, qzeros, G, N, K,
-                                               (uint4 *)out);
+        launch_dequant_t<0>(routine, grid, s, qweight, (const uint16_t *)scales, qzeros, G, N, K, (uint4 *)out);
     else
-        dequant_kernel<1><<<grid, 256, 0, s>>>(qweight, (const uint16_t *)scales, qzeros, G, N, K,
-                                               (uint4 *)out);
+        launch_dequant_t<1>(routine, grid, s, qweight, (const uint16_t *)scales, qzeros, G, N, K, (uint4 *)out);
     return cudaGetLastError();
 }
 

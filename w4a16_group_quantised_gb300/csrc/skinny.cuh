@@ -65,11 +65,10 @@ __device__ __forceinline__ float chain_sum(const float (&acc)[NC][4], int e) {
     return acc[0][e] + acc[1][e];
 }
 
-// zhi2 from zlo2: the same zero point moved from the low-magic to the
-// high-magic position in both lanes.
+// zhi2 from zlo2 (see dequant.cuh).
 template <int DT>
 __device__ __forceinline__ uint32_t zhi_from_zlo(uint32_t zl2) {
-    return ((zl2 & 0x000F000Fu) << (DT == 0 ? 4 : 3)) | rep2(Dtype<DT>::kMagicHi);
+    return zhi_from_zlo_dq<DT>(zl2);
 }
 
 template <int DT>
