@@ -29,6 +29,7 @@ import hashlib
 import json
 import os
 import statistics
+import subprocess
 import sys
 import threading
 import time
@@ -46,6 +47,7 @@ METRIC = ("M=1 decode weight-stream GB/s (% HBM peak); "
 DECODE_WORKLOAD = "qwen3-4b-decode-m1-sym-g128-bf16"
 PREFILL_WORKLOAD = "llama-3.1-8b-prefill-m1920-asym-g64-bf16"
 L2_BYTES_FALLBACK = 126 * 1024 * 1024
+NOMINAL_HBM_GBS = 8000.0     # the nominal "~8 TB/s" of HBM3e, shown beside the measured peak
 
 
 # ----------------------------------------------------------------- helpers
@@ -100,7 +102,7 @@ class ClockSampler:
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, device_index=0, period_s=0.002):
+    def __init__(self, device_index=0, period_s=0.0005):
         self.period = period_s
         self.samples = []
         self.reasons = set()
@@ -123,20 +125,25 @@ class ClockSampler:
         except Exception:
             self.ok = False
 
-    def _run(self):
+    def sample(self):
         clk = ctypes.c_uint()
         rs = ctypes.c_ulonglong()
+        if self.nvml.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk)) == 0:
+            self.samples.append(clk.value)
+        if self.nvml.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(rs)) == 0:
+            for bit, name in self.REASONS.items():
+                if rs.value & bit:
+                    self.reasons.add(name)
+
+    def _run(self):
         while not self._stop.is_set():
-            if self.nvml.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk)) == 0:
-                self.samples.append(clk.value)
-            if self.nvml.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(rs)) == 0:
-                for bit, name in self.REASONS.items():
-                    if rs.value & bit:
-                        self.reasons.add(name)
+            self.sample()
             time.sleep(self.period)
 
     def __enter__(self):
         if self.ok:
+            self.sample()
+            self._stop.clear()
             self._t = threading.Thread(target=self._run, daemon=True)
             self._t.start()
         return self
@@ -145,6 +152,7 @@ class ClockSampler:
         if self.ok:
             self._stop.set()
             self._t.join()
+            self.sample()
 
     def summary(self):
         if not self.ok or not self.samples:
@@ -191,12 +199,15 @@ def upload(w, p):
                 sym=p.sym, dtype=p.dtype)
 
 
-def make_sets(w, make, n_sets, shapes_count):
-    """n_sets weight sets of the same layers.  Set 0 comes from the seeded
-    generator; the others are copies with bytes permuted by a cheap device
-    roll so that every set is distinct memory (the values are equally
+def layer_bytes(d):
+    return decode_bytes(d["M"], d["N"], d["K"], d["G"], d["sym"])
+
+
+def rotated_sets(base, n_sets):
+    """n_sets weight sets of the same layers.  Set 0 is `base` (from the
+    seeded generator); the others are copies with bytes permuted by a cheap
+    device roll so that every set is distinct memory (the values are equally
     distributed)."""
-    base = [upload(w, make(i)) for i in range(shapes_count)]
     sets = [base]
     for s in range(1, n_sets):
         cur = []
@@ -211,80 +222,117 @@ def make_sets(w, make, n_sets, shapes_count):
     return sets
 
 
-def run_step(w, layers, outs):
-    for d, o in zip(layers, outs):
-        w.w4a16_gemm(d["x"], d["qweight"], d["scales"], d["qzeros"], d["G"], out=o)
+def make_sets(w, make, n_sets, shapes_count):
+    return rotated_sets([upload(w, make(i)) for i in range(shapes_count)], n_sets)
 
 
-def bench_decode(w, steps, warmup, l2_bytes):
-    shapes = wl.QWEN3_4B_SHAPES
-    step_bytes = sum(decode_bytes(1, N, K, 128, True) for (_, N, K) in shapes)
-    n_sets = max(2, int(np.ceil(3 * l2_bytes / step_bytes)) + 1)
-    sets = make_sets(w, lambda i: wl.qwen3_4b_decode(i, 1), n_sets, len(shapes))
-    outs = [torch.empty((1, N), dtype=torch.bfloat16, device="cuda") for (_, N, K) in shapes]
-    stream = torch.cuda.Stream()
-    # One CUDA graph holds `chunk` consecutive steps (rotating sets); the
-    # timed region replays it.
-    chunk = n_sets * max(1, 64 // n_sets)
-    with torch.cuda.stream(stream):
-        for s in range(n_sets):   # first calls outside capture (per-device set-up)
-            run_step(w, sets[s], outs)
+def run_step(w, layers, outs, only=None):
+    for i, (d, o) in enumerate(zip(layers, outs)):
+        if only is None or i == only:
+            w.w4a16_gemm(d["x"], d["qweight"], d["scales"], d["qzeros"], d["G"], out=o)
+
+
+class LayerStream:
+    """The layers of one workload, in rotating weight sets larger than 3x the
+    L2 together (every launch streams its weights from HBM), launched from
+    CUDA graphs on a side stream.  A graph of `chunk` steps ends on the set it
+    started from (chunk is a multiple of the set count), so replays rotate.
+    Every graph is replayed once right after capture, so no timed replay is a
+    graph's first."""
+
+    def __init__(self, w, base, l2_bytes, launches_target=64):
+        self.w = w
+        self.step_bytes = sum(layer_bytes(d) for d in base)
+        self.layer_bytes = [layer_bytes(d) for d in base]
+        self.n_sets = max(2, int(np.ceil(3 * l2_bytes / self.step_bytes)) + 1)
+        self.sets = rotated_sets(base, self.n_sets)
+        td = torch.float16 if base[0]["dtype"] == 0 else torch.bfloat16
+        self.outs = [torch.empty((d["M"], d["N"]), dtype=td, device="cuda") for d in base]
+        self.stream = torch.cuda.Stream()
+        self.chunk = self.n_sets * max(1, launches_target // self.n_sets)
+        self.graphs = {}
+        with torch.cuda.stream(self.stream):
+            for s in range(self.n_sets):   # first calls outside capture (per-device set-up)
+                run_step(w, self.sets[s], self.outs)
         torch.cuda.synchronize()
 
-    def capture(n):
-        # n consecutive steps; a graph of `chunk` steps ends on the set it
-        # started from (chunk is a multiple of n_sets), so replays rotate.
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            with torch.cuda.graph(g, stream=stream):
-                for i in range(n):
-                    run_step(w, sets[i % n_sets], outs)
-        return g
+    def graph(self, n, only=None):
+        key = (n, only)
+        if key not in self.graphs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(self.stream):
+                with torch.cuda.graph(g, stream=self.stream):
+                    for i in range(n):
+                        run_step(self.w, self.sets[i % self.n_sets], self.outs, only)
+                g.replay()
+            torch.cuda.synchronize()
+            self.graphs[key] = g
+        return self.graphs[key]
 
-    graphs = {chunk: capture(chunk)}
-    for n in {steps % chunk, warmup % chunk} - {0}:
-        graphs[n] = capture(n)
-    ctx = dict(graphs=graphs, stream=stream, chunk=chunk, steps=steps, step_bytes=step_bytes,
-               n_sets=n_sets, sets=sets, outs=outs, launches_per_step=len(shapes))
-    replay_steps(ctx, warmup)
-    torch.cuda.synchronize()
-    return ctx
+    def prepare(self, *counts):
+        for n in counts:
+            if n % self.chunk:
+                self.graph(n % self.chunk)
+        self.graph(self.chunk)
+
+    def replay_steps(self, n, only=None):
+        """Exactly n steps: n // chunk replays of the chunk graph, then one
+        replay of the graph of the remaining steps."""
+        with torch.cuda.stream(self.stream):   # replay() launches on the current stream
+            for _ in range(n // self.chunk):
+                self.graph(self.chunk, only).replay()
+            if n % self.chunk:
+                self.graph(n % self.chunk, only).replay()
+
+    def timed(self, n, ws=1, only=None):
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        barrier(ws)
+        torch.cuda.synchronize()
+        start.record(self.stream)
+        self.replay_steps(n, only)
+        end.record(self.stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        return start.elapsed_time(end) / 1000.0
+
+    def median_step_s(self, reps=20, only=None):
+        """Median over `reps` replays of the chunk graph, per step."""
+        self.graph(self.chunk, only)
+        return statistics.median(self.timed(self.chunk, 1, only) for _ in range(reps)) / self.chunk
+
+    def per_layer(self, reps=20):
+        """Each layer alone (single-launch timing per shape): median seconds
+        per launch and GB/s."""
+        out = []
+        for i, b in enumerate(self.layer_bytes):
+            t = self.median_step_s(reps, only=i)
+            out.append((t, b / t / 1e9))
+        return out
 
 
-def replay_steps(ctx, n):
-    """Exactly n steps: n // chunk replays of the chunk graph, then one replay
-    of the graph of the remaining steps."""
-    chunk, graphs = ctx["chunk"], ctx["graphs"]
-    with torch.cuda.stream(ctx["stream"]):   # replay() launches on the current stream
-        for _ in range(n // chunk):
-            graphs[chunk].replay()
-        if n % chunk:
-            graphs[n % chunk].replay()
+def stream_summary(st, hbm, layer_names, reps=20):
+    """Whole-step median (the layer stream) and per-shape figures of one
+    LayerStream."""
+    t_step = st.median_step_s(reps)
+    per = st.per_layer(reps)
+    gbs = st.step_bytes / t_step / 1e9
+    return {"step_us": round(t_step * 1e6, 3), "GB/s": round(gbs, 1), "frac": round(gbs / hbm, 4),
+            "frac_nominal_8000": round(gbs / NOMINAL_HBM_GBS, 4), "step_bytes": st.step_bytes,
+            "per_shape": {name: {"us": round(t * 1e6, 3), "GB/s": round(g, 1), "frac": round(g / hbm, 4),
+                                 "bytes": b}
+                          for name, (t, g), b in zip(layer_names, per, st.layer_bytes)}}
 
 
-def timed_replays(ctx, ws):
-    stream = ctx["stream"]
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    barrier(ws)
-    torch.cuda.synchronize()
-    start.record(stream)
-    replay_steps(ctx, ctx["steps"])
-    end.record(stream)
-    torch.cuda.synchronize()
-    barrier(ws)
-    return start.elapsed_time(end) / 1000.0
-
-
-def bench_decode_e2e(w, ctx, steps):
+def bench_decode_e2e(w, st, steps):
     """Through w4a16_gemm_host: pinned x in, y out, per layer, every step."""
-    layers = ctx["sets"][0]
+    layers = st.sets[0]
     xs = [d["x"].cpu().pin_memory() for d in layers]
-    ys = [torch.empty((1, d["N"]), dtype=torch.bfloat16).pin_memory() for d in layers]
+    ys = [torch.empty((d["M"], d["N"]), dtype=d["x"].dtype).pin_memory() for d in layers]
     dx = [torch.empty_like(d["x"]) for d in layers]
-    dy = [torch.empty((1, d["N"]), dtype=torch.bfloat16, device="cuda") for d in layers]
-    h2d = sum(x.numel() * 2 for x in xs)
-    d2h = sum(y.numel() * 2 for y in ys)
+    dy = [torch.empty((d["M"], d["N"]), dtype=d["x"].dtype, device="cuda") for d in layers]
+    h2d = sum(x.numel() * x.element_size() for x in xs)
+    d2h = sum(y.numel() * y.element_size() for y in ys)
     n = max(3, min(steps, 2000))
     for _ in range(3):
         for d, x, y, a, b in zip(layers, xs, ys, dx, dy):
@@ -292,46 +340,43 @@ def bench_decode_e2e(w, ctx, steps):
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(n):
-        layers_i = ctx["sets"][i % ctx["n_sets"]]
+        layers_i = st.sets[i % st.n_sets]
         for d, x, y, a, b in zip(layers_i, xs, ys, dx, dy):
             w.w4a16_gemm_host(x, d["qweight"], d["scales"], d["qzeros"], d["G"], y, a, b)
     dt = (time.perf_counter() - t0) / n
     return dict(dt=dt, h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h, steps=n)
 
 
-def bench_prefill(w, steps):
+def bench_prefill(w, steps, reps=5):
+    """M = 1920 prefill on the four Llama-3.1-8B-shaped layers (one weight set:
+    the contraction is compute-bound, ~0.1-0.4 ms per launch).  Per shape:
+    median over `reps` regions of `steps` back-to-back launches; the step: the
+    four layers in order, same median."""
     shapes = wl.LLAMA31_8B_SHAPES
     layers = [upload(w, wl.llama31_8b_prefill(i, 1920)) for i in range(len(shapes))]
     outs = [torch.empty((1920, N), dtype=torch.bfloat16, device="cuda") for (_, N, K) in shapes]
-    flops = sum(2 * 1920 * N * K for (_, N, K) in shapes)
+    flops = [2 * 1920 * N * K for (_, N, K) in shapes]
     stream = torch.cuda.Stream()
+
+    def region(only):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            run_step(w, layers, outs, only)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1000.0 / steps
+
     with torch.cuda.stream(stream):
         for _ in range(3):
             run_step(w, layers, outs)
         torch.cuda.synchronize()
-        start = torch.cuda.Event(enable_timing=True)
-        end = torch.cuda.Event(enable_timing=True)
-        # per-shape timing for the roofline of the dominant (largest) GEMM
-        per = []
-        for d, o in zip(layers, outs):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(steps):
-                w.w4a16_gemm(d["x"], d["qweight"], d["scales"], d["qzeros"], d["G"], out=o)
-            e1.record(stream)
-            per.append((e0, e1))
-        start.record(stream)
-        for _ in range(steps):
-            run_step(w, layers, outs)
-        end.record(stream)
-    torch.cuda.synchronize()
-    dt = start.elapsed_time(end) / 1000.0 / steps
-    per_ms = [a.elapsed_time(b) / steps for (a, b) in per]
+        per_s = [statistics.median(region(i) for _ in range(reps)) for i in range(len(shapes))]
+        dt = statistics.median(region(None) for _ in range(reps))
     del layers, outs
-    return dict(tflops=flops / dt / 1e12, ms_per_step=dt * 1e3, flops_per_step=flops,
-                per_shape_ms=per_ms,
-                per_shape_tflops=[2 * 1920 * N * K / (ms / 1e3) / 1e12
-                                  for (ms, (_, N, K)) in zip(per_ms, shapes)])
+    return dict(tflops=sum(flops) / dt / 1e12, ms_per_step=dt * 1e3, flops_per_step=sum(flops),
+                per_shape_ms=[t * 1e3 for t in per_s],
+                per_shape_tflops=[f / t / 1e12 for f, t in zip(flops, per_s)])
 
 
 def profile_case(w, which, steps, warmup, m=None):
@@ -420,7 +465,18 @@ def cpu_baseline(sample_steps=None, budget_s=15.0):
     dt = (time.perf_counter() - t0) / n
     return dict(value=step_bytes / dt / 1e9, unit="GB/s", cores=oracle.num_threads(), kind="oracle",
                 sample=f"{n} whole decode steps (4 Qwen3-4B-shaped layers, M=1) in fp64 C",
-                s_per_step=dt)
+                s_per_step=dt, nproc=os.cpu_count())
+
+
+def cpu_baseline_single_thread(budget_s):
+    """The same oracle timing in a child process with one OpenMP thread."""
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-only",
+                        "--cpu-budget", str(budget_s)], env=env, capture_output=True, text=True,
+                       timeout=budget_s * 20 + 300)
+    if r.returncode != 0:
+        return {"error": (r.stderr or r.stdout).strip().splitlines()[-1:]}
+    return json.loads(r.stdout.strip().splitlines()[-1])
 
 
 def reference_arm(steps, warmup, budget_s=150.0):
@@ -466,6 +522,24 @@ def reference_arm(steps, warmup, budget_s=150.0):
                 sample=sample, s_per_step=dt / max(steps, 1))
 
 
+def decode_config(ws):
+    """The `config` of the headline line; both arms print this same dict."""
+    return {"workload": DECODE_WORKLOAD, "M": 1,
+            "layers": "qkv 6144x2560, o_proj 2560x4096, gate_up 19456x2560, down 2560x9728",
+            "G": 128, "quant": "uint4b8 (symmetric)", "act": "bf16",
+            "l2": "rotating weight sets larger than 3x L2",
+            "parallelism": "replicas" if ws > 1 else "single-gpu"}
+
+
+def extra_decode(w, make, shapes, M, l2, hbm):
+    base = [upload(w, make(i, M)) for i in range(len(shapes))]
+    st = LayerStream(w, base, l2)
+    out = stream_summary(st, hbm, [n for (n, _, _) in shapes])
+    del st, base
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -475,13 +549,20 @@ def main():
     ap.add_argument("--prefill-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the extra workloads (Llama decode, M sweep, M=128 prefill)")
     ap.add_argument("--profile-case", choices=["decode", "prefill"],
                     help="run only the short eager case that ncu captures")
     ap.add_argument("--profile-m", type=int, default=None,
                     help="batch size of the --profile-case workload (default: its own)")
     ap.add_argument("--crossover", action="store_true",
                     help="time both kernels at M = 1..16 (the dispatcher's threshold sweep)")
+    ap.add_argument("--cpu-baseline-only", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.cpu_baseline_only:
+        print(json.dumps(cpu_baseline(sample_steps=None, budget_s=args.cpu_budget)))
+        return
     warmup = max(3, args.warmup)
     steps = max(1, args.steps)
     ws, rank, local = dist_info()
@@ -494,9 +575,7 @@ def main():
         line = {"metric": METRIC, "value": round(cb["value"], 4), "unit": "GB/s", "n_gpus": args.gpus,
                 "steps": max(args.steps, 1), "warmup": max(args.warmup, 0), "ms_per_step": cb["s_per_step"] * 1e3,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic", "impl": "reference",
-                "config": {"workload": DECODE_WORKLOAD, "M": 1, "layers": "qkv,o_proj,gate_up,down",
-                           "G": 128, "quant": "uint4b8", "act": "bf16"},
+                "data": "synthetic", "impl": "reference", "config": decode_config(ws),
                 "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
                 "e2e": {"value": round(cb["value"], 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
@@ -520,30 +599,63 @@ def main():
         return
 
     l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size or L2_BYTES_FALLBACK
-    ctx = bench_decode(w, steps, warmup, l2)
+    qshapes = wl.QWEN3_4B_SHAPES
+    st = LayerStream(w, [upload(w, wl.qwen3_4b_decode(i, 1)) for i in range(len(qshapes))], l2)
+    st.prepare(steps, warmup)
+    st.replay_steps(warmup)
+    torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:
-        dt = timed_replays(ctx, ws)
+        dt = st.timed(steps, ws)
+    # A short timed region yields few clock samples: keep sampling over
+    # about 0.3 s more of the same replays (untimed) right after it.
+    soak = None
+    if dt < 0.3:
+        per_chunk = max(dt / steps * st.chunk, 1e-6)
+        n_soak = st.chunk * int(np.ceil(0.3 / per_chunk))
+        with ClockSampler(torch.cuda.current_device()) as soak:
+            st.replay_steps(n_soak)
+            torch.cuda.synchronize()
     dt = max_over_ranks(dt, ws)
     ms_per_step = dt / steps * 1e3
-    value = ctx["step_bytes"] * steps * ws / dt / 1e9
-    launches = steps * ctx["launches_per_step"]
+    value = st.step_bytes * steps * ws / dt / 1e9
+    launches = steps * len(qshapes)
     per_launch_s = dt / launches
-    achieved = ctx["step_bytes"] / ctx["launches_per_step"] / per_launch_s / 1e9
+    achieved = st.step_bytes / len(qshapes) / per_launch_s / 1e9
+    qsum = stream_summary(st, hbm, [n for (n, _, _) in qshapes])
 
     e2e = None
     if not args.no_e2e:
-        r = bench_decode_e2e(w, ctx, min(args.steps, 500))
+        r = bench_decode_e2e(w, st, min(args.steps, 500))
         edt = max_over_ranks(r["dt"], ws)
-        e2e = dict(value=ctx["step_bytes"] * ws / edt / 1e9, unit="GB/s",
+        e2e = dict(value=st.step_bytes * ws / edt / 1e9, unit="GB/s",
                    h2d_bytes_per_step=r["h2d_bytes_per_step"],
                    d2h_bytes_per_step=r["d2h_bytes_per_step"], steps=r["steps"],
                    ms_per_step=edt * 1e3, api="w4a16_gemm_host per layer (pinned host x in, y out)")
-    del ctx
+    del st
     torch.cuda.empty_cache()
+
+    extra = {}
+    if not args.no_extra:
+        lshapes = wl.LLAMA31_8B_SHAPES
+        extra["decode_llama31_8b_m1"] = dict(
+            workload="llama-3.1-8b-decode-m1-asym-g128-fp16",
+            **extra_decode(w, wl.llama31_8b_decode, lshapes, 1, l2, hbm))
+        sweep = {}
+        for M in (2, 3, 4, 5):
+            for tag, make, shp in (("qwen3-4b", wl.qwen3_4b_decode, qshapes),
+                                   ("llama-3.1-8b", wl.llama31_8b_decode, lshapes)):
+                r = extra_decode(w, make, shp, M, l2, hbm)
+                sweep[f"{tag} M={M}"] = {"step_us": r["step_us"], "GB/s": r["GB/s"], "frac": r["frac"],
+                                         "per_shape_GB/s": {k: v["GB/s"] for k, v in r["per_shape"].items()}}
+        extra["decode_m_sweep"] = sweep
+        r = extra_decode(w, wl.llama31_8b_prefill, lshapes, 128, l2, hbm)
+        for name, N, K in lshapes:
+            r["per_shape"][name]["TFLOP/s"] = round(2 * 128 * N * K / (r["per_shape"][name]["us"] * 1e-6) / 1e12, 1)
+        r["TFLOP/s"] = round(sum(2 * 128 * N * K for (_, N, K) in lshapes) / (r["step_us"] * 1e-6) / 1e12, 1)
+        extra["prefill_llama31_8b_m128"] = dict(workload="llama-3.1-8b-prefill-m128-asym-g64-bf16", **r)
 
     pre = bench_prefill(w, max(2, args.prefill_steps))
     dom = int(np.argmax(pre["per_shape_ms"]))
-    tc_peak = tc_sus if tc_sus else tc
 
     dec_hash = source_hash("decode.cu", "skinny.cuh", "dequant.cuh", "ptx.cuh")
     pre_hash = source_hash("prefill.cu", "dequant.cuh", "ptx.cuh")
@@ -554,7 +666,20 @@ def main():
     cb = None
     if not args.no_cpu_baseline:
         c = cpu_baseline(sample_steps=None, budget_s=12.0)
-        cb = {k: c[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        cb = {k: c[k] for k in ("value", "unit", "cores", "kind", "sample", "nproc")}
+        cb["single_thread"] = cpu_baseline_single_thread(8.0)
+    clocks = clk.summary()
+    if soak is not None:
+        ss = soak.summary()
+        clocks["timed_region_samples"] = clocks.pop("samples")
+        clocks["soak_samples"] = ss["samples"]
+        clocks["soak_sm_mhz"] = ss["sm_mhz"]
+        clocks["soak_reasons"] = ss["reasons"]
+        clocks["reasons"] = sorted(set(clocks["reasons"]) | set(ss["reasons"]))
+        if ss["sm_mhz"] is not None:
+            clocks["sm_mhz"] = statistics.median(clk.samples + soak.samples)
+        clocks["note"] = ("timed region shorter than 0.3 s: sm_mhz is the median over it and ~0.3 s "
+                          "of the same replays right after it")
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -568,34 +693,40 @@ def main():
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": DECODE_WORKLOAD, "M": 1, "layers": "qkv 6144x2560, o_proj 2560x4096, "
-                   "gate_up 19456x2560, down 2560x9728", "G": 128, "quant": "uint4b8 (symmetric)",
-                   "act": "bf16", "l2": "rotating weight sets larger than 3x L2",
-                   "parallelism": "replicas" if ws > 1 else "single-gpu",
-                   "launch": "CUDA graph of whole steps, programmatic dependent launch"},
+        "config": decode_config(ws),
+        "launch": "CUDA graphs of whole steps, programmatic dependent launch; every graph replayed once before timing",
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "peak_source": peak_src,
+                     "frac_nominal_8000": round(achieved / NOMINAL_HBM_GBS, 4),
                      "traffic": profiled_traffic("decode_qwen3_4b_m1", dec_hash),
-                     "kernel": "decode_kernel (split-K skinny GEMM)",
-                     "per_launch_us": round(per_launch_s * 1e6, 3)},
+                     "kernel": "decode_kernel (split-K skinny GEMM; all four launches)",
+                     "per_launch_us": round(per_launch_s * 1e6, 3),
+                     "bytes_per_launch": st_bytes_mean(qshapes)},
+        "decode_median": qsum,
         "prefill": {"workload": PREFILL_WORKLOAD, "value": round(pre["tflops"], 2), "unit": "TFLOP/s",
                     "ms_per_step": round(pre["ms_per_step"], 4),
-                    "per_shape_tflops": [round(v, 1) for v in pre["per_shape_tflops"]],
+                    "per_shape_tflops": {n: round(v, 1) for (n, _, _), v in
+                                         zip(wl.LLAMA31_8B_SHAPES, pre["per_shape_tflops"])},
                     "roofline": {"bound": "tensor", "achieved": round(pre["per_shape_tflops"][dom], 2),
-                                 "peak": tc_peak, "unit": "TFLOP/s",
-                                 "frac": round(pre["per_shape_tflops"][dom] / tc_peak, 4),
-                                 "peak_source": peak_src + (" sustained" if tc_sus else ""),
+                                 "peak": tc, "unit": "TFLOP/s",
+                                 "frac": round(pre["per_shape_tflops"][dom] / tc, 4),
+                                 "peak_source": peak_src + " burst (launches of ~0.4 ms timed in short regions)",
                                  "traffic": profiled_traffic("prefill_llama_gate_up_m1920", pre_hash),
                                  "kernel": f"prefill_kernel, {wl.LLAMA31_8B_SHAPES[dom][0]}"}},
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "gpu_launches": launches,
         "device_status": status,
     }
+    line.update(extra)
     if e2e is not None:
         line["e2e"] = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in e2e.items()}
     if cb is not None:
         line["cpu_baseline"] = cb
     print(json.dumps(line))
+
+
+def st_bytes_mean(shapes):
+    return int(sum(decode_bytes(1, N, K, 128, True) for (_, N, K) in shapes) / len(shapes))
 
 
 if __name__ == "__main__":
