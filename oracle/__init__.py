@@ -68,6 +68,7 @@ def _load():
             lib.oracle_round_array.argtypes = [P, ctypes.c_longlong, I, P]
             lib.oracle_half_array_to_double.argtypes = [P, ctypes.c_longlong, I, P]
             lib.oracle_num_threads.restype = I
+            lib.oracle_epilogue.argtypes = [P, I, I, P, I, I, P]
             _lib = lib
     return _lib
 
@@ -171,6 +172,18 @@ def gemm(x, M: int, K: int, qweight, scales, qzeros, G: int, N: int, dtype: int,
                              dtype, _ptr(r), 0 if r is None else r.size,
                              1 if exact_weights else 0, _ptr(y))
     return y
+
+
+def epilogue(y, N: int, dtype: int, bias=None, silu_mul: bool = False) -> np.ndarray:
+    """The fused epilogue on float64 accumulations y [R, N]: + bias (uint16
+    bits [N] or None), then optionally SiLU(gate) * up over the two column
+    halves.  Float64 [R, N] or [R, N / 2]."""
+    y = _c(y, np.float64)
+    R = y.shape[0]
+    b = None if bias is None else _c(bias, np.uint16)
+    out = np.empty((R, N // 2 if silu_mul else N), dtype=np.float64)
+    _load().oracle_epilogue(_ptr(y), R, N, _ptr(b), dtype, 1 if silu_mul else 0, _ptr(out))
+    return out
 
 
 def num_threads() -> int:

@@ -234,6 +234,36 @@ void oracle_gemm(const uint16_t *x, int M, int K, const int32_t *qweight,
     oracle_gemm_rows(x, M, K, qweight, scales, qzeros, G, N, dtype, NULL, 0, 0, y);
 }
 
+/* ---- fused epilogues --------------------------------------------------------
+ * The steps the layer may fuse after its GEMM, on the unrounded binary64
+ * accumulations y [R, N]:
+ *  - bias (the optional `bias` operand of the skinny GEMM call in "Upstream
+ *    sync 67/N: merge 382bbd5144 HybridW4A16LinearKernel (conflict)",
+ *    section "Upstream's Python side is kept"): a[r, n] = y[r, n] + b[n],
+ *    b[n] the exact value of the 16-bit bias pattern; no bias: a = y;
+ *  - SiLU-and-multiply over a merged gate/up projection (N = 2 I, the gate
+ *    rows first): h[r, j] = silu(a[r, j]) * a[r, I + j] with
+ *    silu(v) = v / (1 + exp(-v)), every step in binary64.
+ * out holds [R, N] (no activation) or [R, N / 2] (SiLU-and-multiply); the
+ * library rounds each result once into the activation dtype. */
+void oracle_epilogue(const double *y, int R, int N, const uint16_t *bias, int dtype,
+                     int silu_mul, double *out) {
+    const int I = N / 2;
+    for (int r = 0; r < R; ++r) {
+        const double *yr = y + (size_t)r * N;
+        if (!silu_mul) {
+            for (int n = 0; n < N; ++n)
+                out[(size_t)r * N + n] = yr[n] + (bias ? oracle_half_to_double(bias[n], dtype) : 0.0);
+        } else {
+            for (int j = 0; j < I; ++j) {
+                double g = yr[j] + (bias ? oracle_half_to_double(bias[j], dtype) : 0.0);
+                double u = yr[I + j] + (bias ? oracle_half_to_double(bias[I + j], dtype) : 0.0);
+                out[(size_t)r * I + j] = g / (1.0 + exp(-g)) * u;
+            }
+        }
+    }
+}
+
 /* Output rounding: RN_dtype of each double (the library's output is the
  * fp32 accumulator rounded once into the activation dtype). */
 void oracle_round_array(const double *v, long long n, int dtype, uint16_t *out) {

@@ -268,3 +268,58 @@ def test_rows_subset_and_exact_weights_flag():
     ye = oracle.gemm(p.x, 3, 64, qw, p.scales, qz, 32, 8, BF16, exact_weights=True)
     assert not np.array_equal(y, ye)           # bf16 weight rounding is visible
     np.testing.assert_allclose(y, ye, rtol=0.05, atol=0.05)
+
+
+# --------------------------------------------------------------------- fused epilogue
+def test_epilogue_bias_closed_forms():
+    """With x = 0 the layer output is the bias itself (exact values of its
+    bit patterns); adding a bias shifts every row by the same vector."""
+    p = make_problem(3, 16, 64, 32, False, F16, seed=41)
+    bias = np.array([0x3C00, 0xBC00, 0x3800, 0x0001, 0x7BFF, 0, 0x8000, 0x4248] * 2, dtype=np.uint16)
+    zero_x = np.zeros_like(p.x)
+    qw = oracle.pack(p.q)
+    qz = oracle.pack_zeros(p.z)
+    y0 = oracle.gemm(zero_x, 3, 64, qw, p.scales, qz, 32, 16, F16)
+    a0 = oracle.epilogue(y0, 16, F16, bias=bias)
+    want = bias.view(np.float16).astype(np.float64)
+    assert np.array_equal(a0, np.tile(want, (3, 1)))
+    y = oracle.gemm(p.x, 3, 64, qw, p.scales, qz, 32, 16, F16)
+    a = oracle.epilogue(y, 16, F16, bias=bias)
+    np.testing.assert_allclose(a - y, np.tile(want, (3, 1)), rtol=0, atol=1e-12 * (1 + np.abs(y).max()))
+    assert np.array_equal(oracle.epilogue(y, 16, F16), y)
+
+
+def test_epilogue_silu_special_values():
+    """sigmoid(ln 3) = 3/4 and sigmoid(-ln 3) = 1/4, so silu(+-ln 3) =
+    +-(3/4 or -1/4) ln 3; silu(0) = 0; silu(v) - silu(-v) = v for every v
+    (sigmoid(v) + sigmoid(-v) = 1); the up half multiplies column by column."""
+    l3 = np.log(3.0)
+    y = np.array([[0.0, l3, -l3, 2.0, 1.0, 3.0]])
+    h = oracle.epilogue(y, 6, BF16, silu_mul=True)
+    np.testing.assert_allclose(h[0], [0.0, 0.75 * l3 * 1.0, -0.25 * l3 * 3.0], rtol=1e-15, atol=0)
+    v = np.linspace(-30, 30, 241)
+    ypos = np.concatenate([v, np.ones_like(v)])[None, :]
+    yneg = np.concatenate([-v, np.ones_like(v)])[None, :]
+    d = oracle.epilogue(ypos, 482, F16, silu_mul=True) - oracle.epilogue(yneg, 482, F16, silu_mul=True)
+    np.testing.assert_allclose(d[0], v, rtol=0, atol=1e-13)
+
+
+def test_epilogue_silu_mul_against_torch():
+    """The whole epilogue on a real layer's accumulations against torch's
+    SiLU (its own implementation) on the gate half times the up half, with
+    the bias of each half added first."""
+    p = make_problem(4, 64, 128, 64, True, BF16, seed=43)
+    qw = oracle.pack(p.q)
+    y = oracle.gemm(p.x, 4, 128, qw, p.scales, None, 64, 64, BF16)
+    rng = np.random.default_rng(5)
+    bias_f = rng.uniform(-2, 2, 64).astype(np.float32)
+    bias = torch.from_numpy(bias_f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    bv = bias.astype(np.uint32) << 16
+    b64 = bv.view(np.float32).astype(np.float64)
+    h = oracle.epilogue(y, 64, BF16, bias=bias, silu_mul=True)
+    a = torch.from_numpy(y + b64)
+    want = torch.nn.functional.silu(a[:, :32]) * a[:, 32:]
+    np.testing.assert_allclose(h, want.numpy(), rtol=1e-12, atol=1e-12)
+    # the halves are not interchangeable: swapping them changes the result
+    swapped = torch.nn.functional.silu(a[:, 32:]) * a[:, :32]
+    assert not np.allclose(h, swapped.numpy())

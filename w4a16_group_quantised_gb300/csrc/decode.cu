@@ -415,7 +415,9 @@ bool decode_cfg_valid(const DecodeCfg &c, int M, int K, int G, bool asym) {
 // Configuration from measured sweeps on GB300 (M = 1 decode, the Qwen3-4B-
 // and Llama-3.1-8B-shaped layers, CUDA graphs with programmatic dependent
 // launch, both per layer and over the four layers of a step in sequence,
-// where a layer's CTAs must leave room for the next layer's to start early):
+// where a layer's CTAs must leave room for the next layer's to start early;
+// the last search chose each layer's configuration by the time of the whole
+// step, one layer at a time):
 // one 16-row block per warp, 128-k boxes, K split into more cluster CTAs as N
 // shrinks.  The ring is then made as deep as it can be while the whole grid
 // stays resident on the SMs at once (a deeper ring that pushes CTAs into a
@@ -426,9 +428,9 @@ DecodeCfg decode_pick_cfg(int M, int N, int K, int G, int sym, int dtype, int sm
     if (N >= 24576)
         c = DecodeCfg{1, 4, 4, 2, 1};
     else if (N >= 16384)
-        c = DecodeCfg{1, 8, 2, 3, 2};
+        c = DecodeCfg{1, 8, 4, 2, 2};
     else if (N >= 6144)
-        c = DecodeCfg{1, 4, 4, 2, 5};
+        c = K <= 3072 ? DecodeCfg{1, 8, 2, 4, 5} : DecodeCfg{1, 4, 4, 3, 4};
     else
         c = DecodeCfg{1, 4, 4, 4, 8};
     const int nblk = (K + kBoxK - 1) / kBoxK;
