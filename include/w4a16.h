@@ -158,6 +158,62 @@ int w4a16_gemm_ex(const void *x, int M, int K, const int32_t *qweight, const voi
                   const int32_t *qzeros_or_null, int G, int N, void *out,
                   w4a16_stream_t stream, w4a16_dtype_t dtype, w4a16_path_t path);
 
+/* Epilogues the layer can fuse after its GEMM. */
+typedef enum {
+    W4A16_EPI_NONE = 0,      /* out [M, N] = y (+ bias)                        */
+    W4A16_EPI_SILU_MUL = 1   /* out [M, N/2] = silu(y[:, :N/2]) * y[:, N/2:]   */
+} w4a16_epilogue_t;
+
+/* w4a16_gemm_ex with a fused epilogue, in the same launch.
+ * Source: "Upstream sync 67/N: merge 382bbd5144 HybridW4A16LinearKernel
+ * (conflict)", section "Upstream's Python side is kept -- and it does NOT
+ * work here": the skinny GEMM call carries an optional `bias`.  The SiLU-
+ * and-multiply epilogue is the step that follows a merged gate/up projection
+ * in the models the pages benchmark.
+ *  bias_or_null: device [N] in `dtype` (2-byte aligned), added to the fp32
+ *    sums before the one rounding, or NULL;
+ *  epilogue W4A16_EPI_NONE: out [M, N] = RN(x . dequant(W)^T + bias);
+ *  epilogue W4A16_EPI_SILU_MUL: W is a merged gate/up weight, rows 0..N/2-1
+ *    the gate and rows N/2..N-1 the up projection; with g, u those halves'
+ *    fp32 sums plus bias, out [M, N/2] = RN(silu(g) * u), silu(v) =
+ *    v / (1 + exp(-v)).  Runs on the decode kernel only: M must be <=
+ *    W4A16_MAX_DECODE_M and path AUTO or DECODE (else W4A16_ERR_SHAPE /
+ *    W4A16_ERR_ARG).
+ * Other arguments, requirements and errors as w4a16_gemm_ex; an unknown
+ * epilogue is W4A16_ERR_ARG. */
+int w4a16_gemm_fused(const void *x, int M, int K, const int32_t *qweight, const void *scales,
+                     const int32_t *qzeros_or_null, int G, int N, const void *bias_or_null,
+                     int epilogue, void *out, w4a16_stream_t stream, w4a16_dtype_t dtype,
+                     w4a16_path_t path);
+
+/* One layer of a chain (w4a16_gemm_chain): its weights, optional bias,
+ * epilogue and output buffer.  N, K and G as in w4a16_gemm. */
+typedef struct {
+    const int32_t *qweight;
+    const void *scales;
+    const int32_t *qzeros_or_null;
+    const void *bias_or_null;
+    int G, N, K;
+    int epilogue;            /* w4a16_epilogue_t */
+    void *out;               /* [M, N] or, with W4A16_EPI_SILU_MUL, [M, N/2] */
+} w4a16_layer_t;
+
+/* A stream of linear layers in which layer i's output is layer i+1's input:
+ * layer 0 reads x [M, layers[0].K]; layer i > 0 reads layers[i-1].out, so
+ * layers[i].K must equal layer i-1's output width (W4A16_ERR_SHAPE
+ * otherwise).  Each layer runs as w4a16_gemm_fused with path AUTO, enqueued
+ * back to back on `stream` with programmatic dependent launch: a layer's
+ * kernel may start while the previous one drains, streaming its own weights,
+ * and reads its input only after the previous kernel has completed.  No
+ * weight, scale, zero-point or bias buffer of the chain may be an output of
+ * it.  Safe to capture in a CUDA graph.  Source: "[ROCm][Kernel] Add
+ * HybridW4A16LinearKernel: Triton prefill + HIP skinny decode", benchmark
+ * tables (per-token decode latency over a model's layer stream).  All
+ * arguments are checked before the first launch; an error then returns
+ * without enqueuing anything. */
+int w4a16_gemm_chain(const void *x, int M, const w4a16_layer_t *layers, int n_layers,
+                     w4a16_dtype_t dtype, w4a16_stream_t stream);
+
 /* End-to-end form: x_host and out_host are HOST buffers (pinned for full
  * speed); x_dev [M, K] and out_dev [M, N] are caller-owned device staging
  * buffers.  Copies x to the device, runs w4a16_gemm, copies y back and

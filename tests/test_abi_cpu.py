@@ -44,6 +44,7 @@ def test_version(lib):
 NULL = None
 ALIGNED = ctypes.c_void_p(0x1000)     # never dereferenced: validation fails first
 MISALIGNED = ctypes.c_void_p(0x1008)
+ODD = ctypes.c_void_p(0x1001)
 
 
 def gemm(lib, x=ALIGNED, M=1, K=128, qw=ALIGNED, s=ALIGNED, qz=NULL, G=32, N=64, out=ALIGNED,
@@ -139,11 +140,104 @@ def test_debug_config_validation(lib):
     assert lib.w4a16_debug_set_config(6, None, 0) == -9
 
 
+def test_fused_entry_point_limits(lib):
+    """w4a16_gemm_fused: host validation of the epilogue and bias arguments."""
+    f = lib.w4a16_gemm_fused
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int]
+    args = lambda M=1, bias=None, epi=0, path=0: f(ALIGNED, M, 128, ALIGNED, ALIGNED, None, 32, 64, bias, epi,
+                                                  ALIGNED, None, 0, path)
+    assert args(epi=2) == -9                       # unknown epilogue
+    assert args(epi=1, M=9) == -2                  # SiLU-and-multiply is a decode epilogue
+    assert args(epi=1, path=2) == -9               # ... not on the prefill kernel
+    assert args(bias=ODD) == -4                    # bias must be 2-byte aligned
+    assert args(M=0, epi=1) == 0                   # empty is a no-op
+    assert args(M=0, bias=ALIGNED) == 0
+
+
+def _cpu(*shape, dtype=None):
+    import torch
+    return torch.zeros(*shape, dtype=dtype or torch.float16)
+
+
 def test_binding_rejects_wrong_zero_point_dtype():
     """The packed zero-point contract: int32 only (a float tensor of zero
     points is refused before the library is called)."""
     import torch
-    import w4a16_group_quantised_gb300 as w
+    from w4a16_group_quantised_gb300 import binding as b
     with pytest.raises(TypeError):
-        w.w4a16_gemm(torch.zeros(1, 64, dtype=torch.float16), torch.zeros(8, 8, dtype=torch.int32),
-                      torch.zeros(8, 2, dtype=torch.float16), torch.zeros(1, 2, dtype=torch.float16), 32)
+        b._check_gemm_operands(_cpu(1, 64), _cpu(8, 8, dtype=torch.int32), _cpu(8, 2), _cpu(1, 2), 32, None,
+                               require_cuda=False)
+
+
+def test_binding_operand_checks():
+    """Types, dtypes, shapes, layout and device are checked before the C
+    call: TypeError for a type or dtype, ValueError for the rest."""
+    import torch
+    from w4a16_group_quantised_gb300 import binding as b
+    i32 = torch.int32
+    x, qw, s, qz = _cpu(2, 64), _cpu(16, 8, dtype=i32), _cpu(16, 2), _cpu(2, 2, dtype=i32)
+    ok = dict(require_cuda=False)
+    assert b._check_gemm_operands(x, qw, s, qz, 32, _cpu(2, 16), **ok) == (2, 64, 16)
+    with pytest.raises(ValueError, match="CUDA"):
+        b._check_gemm_operands(x, qw, s, qz, 32, None)                       # CPU tensors
+    with pytest.raises(TypeError):
+        b._check_gemm_operands(x.float(), qw, s, qz, 32, None, **ok)          # fp32 activations
+    with pytest.raises(TypeError):
+        b._check_gemm_operands(x, qw.to(torch.int64), s, qz, 32, None, **ok)  # int64 weights
+    with pytest.raises(TypeError):
+        b._check_gemm_operands(x, qw, s.to(torch.bfloat16), qz, 32, None, **ok)   # scales dtype
+    with pytest.raises(TypeError):
+        b._check_gemm_operands(x, qw, s, qz, 32.0, None, **ok)                 # G not an int
+    with pytest.raises(TypeError):
+        b._check_gemm_operands(x.numpy(), qw, s, qz, 32, None, **ok)           # not a tensor
+    with pytest.raises(ValueError, match="contiguous"):
+        b._check_gemm_operands(_cpu(64, 2).t(), qw, s, qz, 32, None, **ok)
+    with pytest.raises(ValueError, match="qweight"):
+        b._check_gemm_operands(x, _cpu(16, 4, dtype=i32), s, qz, 32, None, **ok)
+    with pytest.raises(ValueError, match="scales"):
+        b._check_gemm_operands(x, qw, _cpu(16, 4), qz, 32, None, **ok)
+    with pytest.raises(ValueError, match="qzeros"):
+        b._check_gemm_operands(x, qw, s, _cpu(16, 2, dtype=i32), 32, None, **ok)
+    with pytest.raises(ValueError, match="out"):
+        b._check_gemm_operands(x, qw, s, qz, 32, _cpu(2, 8), **ok)
+    with pytest.raises(TypeError):
+        b._check_gemm_operands(x, qw, s, qz, 32, _cpu(2, 16, dtype=torch.bfloat16), **ok)
+    with pytest.raises(ValueError, match="bias"):
+        b._check_gemm_operands(x, qw, s, qz, 32, None, bias=_cpu(8), **ok)
+    # SiLU-and-multiply writes [M, N/2]
+    assert b._check_gemm_operands(x, qw, s, None, 32, _cpu(2, 8), out_cols=8, **ok) == (2, 64, 16)
+
+
+class _Layer(ctypes.Structure):
+    _fields_ = [("qweight", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("qzeros_or_null", ctypes.c_void_p), ("bias_or_null", ctypes.c_void_p),
+                ("G", ctypes.c_int), ("N", ctypes.c_int), ("K", ctypes.c_int),
+                ("epilogue", ctypes.c_int), ("out", ctypes.c_void_p)]
+
+
+def test_chain_entry_point_limits(lib):
+    """w4a16_gemm_chain checks the whole chain on the host first: widths must
+    chain (a SiLU-and-multiply layer halves its width), layers non-null."""
+    f = lib.w4a16_gemm_chain
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    a = ALIGNED.value
+
+    def layers(*specs):
+        arr = (_Layer * len(specs))(*[_Layer(a, a, None, None, 32, N, K, epi, a) for (N, K, epi) in specs])
+        return ctypes.cast(arr, ctypes.c_void_p), arr
+
+    p, keep = layers((64, 128, 0), (32, 64, 0))
+    assert f(ALIGNED, 0, p, 2, 0, None) == 0                   # M == 0: nothing to do
+    p, keep = layers((64, 128, 0), (32, 96, 0))
+    assert f(ALIGNED, 1, p, 2, 0, None) == -2                  # 96 != 64
+    p, keep = layers((64, 128, 1), (32, 64, 0))
+    assert f(ALIGNED, 1, p, 2, 0, None) == -2                  # SiLU halves 64 -> 32
+    p, keep = layers((64, 128, 3))
+    assert f(ALIGNED, 1, p, 1, 0, None) == -9                  # unknown epilogue
+    p, keep = layers((64, 128, 1))
+    assert f(ALIGNED, 9, p, 1, 0, None) == -2                  # SiLU needs M <= 8
+    assert f(ALIGNED, 1, None, 2, 0, None) == -1
+    assert f(ALIGNED, 1, None, 0, 0, None) == 0
+    assert f(ALIGNED, 1, None, -1, 0, None) == -9

@@ -11,13 +11,17 @@ into it.  Nothing here falls back to a CPU or PyTorch implementation: if the
 library is missing the calls raise.
 """
 from .binding import (  # noqa: F401
+    EPI_NONE,
+    EPI_SILU_MUL,
     W4A16Error,
     library_path,
     load_library,
     w4a16_debug_set_config,
     w4a16_dequant_debug,
     w4a16_gemm,
+    w4a16_gemm_chain,
     w4a16_gemm_decode_noalloc,
+    w4a16_gemm_fused,
     w4a16_gemm_host,
     w4a16_last_device_error,
     w4a16_pack,

@@ -18,6 +18,7 @@ _lib = None
 
 W4A16_F16, W4A16_BF16 = 0, 1
 PATH_AUTO, PATH_DECODE, PATH_PREFILL = 0, 1, 2
+EPI_NONE, EPI_SILU_MUL = 0, 1
 
 _STATUS = {
     0: "W4A16_OK", -1: "W4A16_ERR_NULL", -2: "W4A16_ERR_SHAPE", -3: "W4A16_ERR_GROUP",
@@ -57,6 +58,8 @@ def load_library():
             "w4a16_gemm_f16": [P, I, I, P, P, P, I, I, P, P],
             "w4a16_gemm_bf16": [P, I, I, P, P, P, I, I, P, P],
             "w4a16_gemm_ex": [P, I, I, P, P, P, I, I, P, P, I, I],
+            "w4a16_gemm_fused": [P, I, I, P, P, P, I, I, P, I, P, P, I, I],
+            "w4a16_gemm_chain": [P, I, P, I, I, P],
             "w4a16_gemm_host": [P, I, I, P, P, P, I, I, P, I, P, P, P],
             "w4a16_gemm_decode_noalloc": [P, I, I, P, P, P, I, I, P, P, I],
             "w4a16_select_path": [I, I, I, I, I, I],
@@ -102,6 +105,58 @@ def _require_int32(name, t):
     if t is not None and t.dtype not in (torch.int32,):
         # The packed zero-point contract: int32, 8 x uint4 along dim 0.
         raise TypeError(f"{name} must be int32 (packed 8 x uint4), got {t.dtype}")
+
+
+def _check_gemm_operands(x, qweight, scales, qzeros, G, out, out_cols=None, bias=None,
+                         require_cuda=True):
+    """Host-side checks of the operands' types, dtypes, shapes, layout and
+    device before the C call (which checks again what it can see: sizes,
+    alignment, G).  TypeError for a wrong type or dtype, ValueError for a
+    wrong shape, layout or device."""
+    import torch
+    named = [("x", x), ("qweight", qweight), ("scales", scales), ("qzeros", qzeros), ("out", out),
+             ("bias", bias)]
+    for name, t in named:
+        if t is None and name in ("qzeros", "out", "bias"):
+            continue
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor, got {type(t).__name__}")
+        if require_cuda and t.device.type != "cuda":
+            raise ValueError(f"{name} must be a CUDA tensor, got device {t.device}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    devs = {t.device for _, t in named if t is not None}
+    if len(devs) > 1:
+        raise ValueError(f"operands are on different devices: {sorted(map(str, devs))}")
+    if not isinstance(G, int) or isinstance(G, bool):
+        raise TypeError(f"G must be an int, got {type(G).__name__}")
+    _dtype_code(x)
+    _require_int32("qweight", qweight)
+    _require_int32("qzeros", qzeros)
+    if x.dim() != 2 or qweight.dim() != 2 or scales.dim() != 2:
+        raise ValueError("x, qweight and scales must be 2-D")
+    M, K = x.shape
+    N = qweight.shape[0]
+    if qweight.shape[1] * 8 != K:
+        raise ValueError(f"qweight must be [N, K/8] = [{N}, {K // 8}], got {list(qweight.shape)}")
+    if scales.dtype != x.dtype:
+        raise TypeError(f"scales dtype {scales.dtype} differs from x dtype {x.dtype}")
+    if G > 0 and K % G == 0 and list(scales.shape) != [N, K // G]:
+        raise ValueError(f"scales must be [N, K/G] = [{N}, {K // G}], got {list(scales.shape)}")
+    if qzeros is not None and G > 0 and K % G == 0 and list(qzeros.shape) != [N // 8, K // G]:
+        raise ValueError(f"qzeros must be [N/8, K/G] = [{N // 8}, {K // G}], got {list(qzeros.shape)}")
+    if bias is not None:
+        if bias.dtype != x.dtype:
+            raise TypeError(f"bias dtype {bias.dtype} differs from x dtype {x.dtype}")
+        if bias.dim() != 1 or bias.shape[0] != N:
+            raise ValueError(f"bias must be [N] = [{N}], got {list(bias.shape)}")
+    if out is not None:
+        cols = N if out_cols is None else out_cols
+        if out.dtype != x.dtype:
+            raise TypeError(f"out dtype {out.dtype} differs from x dtype {x.dtype}")
+        if list(out.shape) != [M, cols]:
+            raise ValueError(f"out must be [{M}, {cols}], got {list(out.shape)}")
+    return M, K, N
 
 
 def w4a16_pack(q, qweight=None, stream=None):
@@ -154,10 +209,7 @@ def w4a16_dequant_debug(qweight, scales, qzeros, G: int, out=None, stream=None, 
 def w4a16_gemm(x, qweight, scales, qzeros, G: int, out=None, stream=None, path: int = PATH_AUTO):
     """y[M, N] = x[M, K] . dequant(W)^T in the dtype of x."""
     import torch
-    _require_int32("qweight", qweight)
-    _require_int32("qzeros", qzeros)
-    M, K = x.shape
-    N = qweight.shape[0]
+    M, K, N = _check_gemm_operands(x, qweight, scales, qzeros, G, out)
     dt = _dtype_code(x)
     if out is None:
         out = torch.empty((M, N), dtype=x.dtype, device=x.device)
@@ -170,6 +222,64 @@ def w4a16_gemm(x, qweight, scales, qzeros, G: int, out=None, stream=None, path: 
                                _stream_ptr(stream), dt, path)
     _check("w4a16_gemm", rc)
     return out
+
+
+def w4a16_gemm_fused(x, qweight, scales, qzeros, G: int, bias=None, epilogue: int = EPI_NONE,
+                     out=None, stream=None, path: int = PATH_AUTO):
+    """x . dequant(W)^T + bias with the epilogue fused: EPI_NONE gives [M, N];
+    EPI_SILU_MUL (W = [gate; up], N = 2 I) gives silu(gate) * up, [M, I]."""
+    import torch
+    if epilogue not in (EPI_NONE, EPI_SILU_MUL):
+        raise ValueError(f"unknown epilogue {epilogue}")
+    N0 = qweight.shape[0] if isinstance(qweight, torch.Tensor) else 0
+    cols = N0 // 2 if epilogue == EPI_SILU_MUL else N0
+    M, K, N = _check_gemm_operands(x, qweight, scales, qzeros, G, out, out_cols=cols, bias=bias)
+    if epilogue == EPI_SILU_MUL and N % 2:
+        raise ValueError("SiLU-and-multiply needs an even number of weight rows")
+    dt = _dtype_code(x)
+    if out is None:
+        out = torch.empty((M, cols), dtype=x.dtype, device=x.device)
+    lib = load_library()
+    rc = lib.w4a16_gemm_fused(_p(x), M, K, _p(qweight), _p(scales), _p(qzeros), G, N, _p(bias), epilogue,
+                              _p(out), _stream_ptr(stream), dt, path)
+    _check("w4a16_gemm_fused", rc)
+    return out
+
+
+class w4a16_layer_t(ctypes.Structure):
+    """Mirror of the C struct w4a16_layer_t (include/w4a16.h)."""
+    _fields_ = [("qweight", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("qzeros_or_null", ctypes.c_void_p), ("bias_or_null", ctypes.c_void_p),
+                ("G", ctypes.c_int), ("N", ctypes.c_int), ("K", ctypes.c_int),
+                ("epilogue", ctypes.c_int), ("out", ctypes.c_void_p)]
+
+
+def w4a16_gemm_chain(x, layers, stream=None):
+    """Run layers back to back, layer i's output feeding layer i+1.  `layers`
+    is a sequence of dicts with qweight, scales, qzeros, G and optionally bias,
+    epilogue and out (created when missing).  Returns the list of outputs."""
+    import torch
+    M = x.shape[0]
+    outs, structs, inp = [], [], x
+    for i, L in enumerate(layers):
+        epi = L.get("epilogue", EPI_NONE)
+        N = L["qweight"].shape[0]
+        cols = N // 2 if epi == EPI_SILU_MUL else N
+        out = L.get("out")
+        if out is None:
+            out = torch.empty((M, cols), dtype=x.dtype, device=x.device)
+        _check_gemm_operands(inp, L["qweight"], L["scales"], L.get("qzeros"), L["G"], out, out_cols=cols,
+                             bias=L.get("bias"))
+        structs.append(w4a16_layer_t(_p(L["qweight"]), _p(L["scales"]), _p(L.get("qzeros")), _p(L.get("bias")),
+                                     L["G"], N, inp.shape[1], epi, _p(out)))
+        outs.append(out)
+        inp = out
+    arr = (w4a16_layer_t * max(1, len(structs)))(*structs)
+    lib = load_library()
+    rc = lib.w4a16_gemm_chain(_p(x), M, ctypes.cast(arr, ctypes.c_void_p), len(structs), _dtype_code(x),
+                              _stream_ptr(stream))
+    _check("w4a16_gemm_chain", rc)
+    return outs
 
 
 def w4a16_gemm_host(x_host, qweight, scales, qzeros, G: int, out_host, dev_x, dev_out,
@@ -194,10 +304,7 @@ def w4a16_gemm_decode_noalloc(x, qweight, scales, qzeros, G: int, out=None, stre
     caller that must not allocate; if it is None a tensor is created here."""
     import torch
     lib = load_library()
-    _require_int32("qzeros", qzeros)
-    _require_int32("qweight", qweight)
-    M, K = x.shape
-    N = qweight.shape[0]
+    M, K, N = _check_gemm_operands(x, qweight, scales, qzeros, G, out)
     if out is None:
         out = torch.empty((M, N), dtype=x.dtype, device=x.device)
     rc = lib.w4a16_gemm_decode_noalloc(_p(x), M, K, _p(qweight), _p(scales),

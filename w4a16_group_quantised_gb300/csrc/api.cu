@@ -223,12 +223,20 @@ int select_path_impl(int M, int N, int K, int G, int sym, int dtype) {
 }
 
 int run_gemm(const void *x, int M, int K, const int32_t *qw, const void *scales, const int32_t *qz,
-             int G, int N, void *out, w4a16_stream_t stream, int dtype, int path) {
+             int G, int N, void *out, w4a16_stream_t stream, int dtype, int path,
+             const void *bias = nullptr, int epilogue = W4A16_EPI_NONE) {
     int rc = validate_gemm(x, M, K, qw, scales, qz, G, N, out, dtype);
     if (rc != W4A16_OK) return rc;
     if (path != W4A16_PATH_AUTO && path != W4A16_PATH_DECODE && path != W4A16_PATH_PREFILL)
         return W4A16_ERR_ARG;
+    if (epilogue != W4A16_EPI_NONE && epilogue != W4A16_EPI_SILU_MUL) return W4A16_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(bias) & 1u) != 0) return W4A16_ERR_ALIGN;
     if (path == W4A16_PATH_DECODE && M > W4A16_MAX_DECODE_M) return W4A16_ERR_SHAPE;
+    if (epilogue == W4A16_EPI_SILU_MUL) {
+        if (path == W4A16_PATH_PREFILL) return W4A16_ERR_ARG;
+        if (M > W4A16_MAX_DECODE_M) return W4A16_ERR_SHAPE;
+        path = W4A16_PATH_DECODE;
+    }
     if (M == 0) return W4A16_OK;
     const DeviceInfo *dev = nullptr;
     DevState *st = nullptr;
@@ -237,6 +245,9 @@ int run_gemm(const void *x, int M, int K, const int32_t *qw, const void *scales,
     if (path == W4A16_PATH_AUTO) path = select_path_impl(M, N, K, G, qz == nullptr, dtype);
 
     GemmArgs a{x, qw, scales, qz, out, M, N, K, G, dtype};
+    a.bias = bias;
+    a.silu_mul = epilogue == W4A16_EPI_SILU_MUL ? 1 : 0;
+    const bool plain = bias == nullptr && epilogue == W4A16_EPI_NONE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool asym = qz != nullptr;
     bool pdl;
@@ -259,7 +270,7 @@ int run_gemm(const void *x, int M, int K, const int32_t *qw, const void *scales,
         }
         float *ws = nullptr;
         int *cnt = nullptr;
-        if (sk_on && (N + 15) / 16 <= kDecodeTickets && decode_sk_applicable(M, K) &&
+        if (plain && sk_on && (N + 15) / 16 <= kDecodeTickets && decode_sk_applicable(M, K) &&
             stream_scratch(*st, s, &ws, &cnt)) {
             e = launch_decode_sk(a, ns_pref, *dev, ws, cnt, s, pdl);
             return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
@@ -386,6 +397,44 @@ int w4a16_gemm_ex(const void *x, int M, int K, const int32_t *qweight, const voi
                   const int32_t *qzeros_or_null, int G, int N, void *out, w4a16_stream_t stream,
                   w4a16_dtype_t dtype, w4a16_path_t path) {
     return run_gemm(x, M, K, qweight, scales, qzeros_or_null, G, N, out, stream, (int)dtype, (int)path);
+}
+
+int w4a16_gemm_fused(const void *x, int M, int K, const int32_t *qweight, const void *scales,
+                     const int32_t *qzeros_or_null, int G, int N, const void *bias_or_null, int epilogue,
+                     void *out, w4a16_stream_t stream, w4a16_dtype_t dtype, w4a16_path_t path) {
+    return run_gemm(x, M, K, qweight, scales, qzeros_or_null, G, N, out, stream, (int)dtype, (int)path,
+                    bias_or_null, epilogue);
+}
+
+int w4a16_gemm_chain(const void *x, int M, const w4a16_layer_t *layers, int n_layers, w4a16_dtype_t dtype,
+                     w4a16_stream_t stream) {
+    if (n_layers < 0) return W4A16_ERR_ARG;
+    if (n_layers > 0 && layers == nullptr) return W4A16_ERR_NULL;
+    // validate the whole chain before enqueuing anything
+    const void *in = x;
+    for (int i = 0; i < n_layers; ++i) {
+        const w4a16_layer_t &L = layers[i];
+        int rc = validate_gemm(in, M, L.K, L.qweight, L.scales, L.qzeros_or_null, L.G, L.N, L.out, (int)dtype);
+        if (rc != W4A16_OK) return rc;
+        if (L.epilogue != W4A16_EPI_NONE && L.epilogue != W4A16_EPI_SILU_MUL) return W4A16_ERR_ARG;
+        if ((reinterpret_cast<uintptr_t>(L.bias_or_null) & 1u) != 0) return W4A16_ERR_ALIGN;
+        if (L.epilogue == W4A16_EPI_SILU_MUL && M > W4A16_MAX_DECODE_M) return W4A16_ERR_SHAPE;
+        if (i > 0) {
+            const w4a16_layer_t &P = layers[i - 1];
+            const int width = P.epilogue == W4A16_EPI_SILU_MUL ? P.N / 2 : P.N;
+            if (L.K != width) return W4A16_ERR_SHAPE;
+        }
+        in = L.out;
+    }
+    in = x;
+    for (int i = 0; i < n_layers; ++i) {
+        const w4a16_layer_t &L = layers[i];
+        int rc = run_gemm(in, M, L.K, L.qweight, L.scales, L.qzeros_or_null, L.G, L.N, L.out, stream, (int)dtype,
+                          W4A16_PATH_AUTO, L.bias_or_null, L.epilogue);
+        if (rc != W4A16_OK) return rc;
+        in = L.out;
+    }
+    return W4A16_OK;
 }
 
 int w4a16_gemm_host(const void *x_host, int M, int K, const int32_t *qweight, const void *scales,

@@ -35,9 +35,15 @@
 //    after it.  Weights, scales and zero points must therefore not be
 //    written by the immediately preceding kernel if that kernel triggers
 //    early launch.
+//  * Fused epilogue: an optional bias [N] is added to the fp32 sums before
+//    the one rounding; with SiLU-and-multiply (a merged gate/up weight of
+//    N = 2 I rows, the gate rows first) a CTA's RT rows are RT / 2 gate rows
+//    j0.. and the RT / 2 up rows I + j0.. (one TMA box over a [2][I] view of
+//    the rows), and it writes silu(gate) * up for its RT / 2 outputs.
 //  * Every mbarrier wait is bounded; on a timeout the status word is set and
 //    the CTA leaves its loop.
 #include <algorithm>
+#include <mutex>
 #include <cooperative_groups.h>
 #include <cuda.h>
 
@@ -58,6 +64,7 @@ struct DecodeParams {
     const uint16_t *scales;
     const int32_t *qz;
     uint16_t *out;
+    const uint16_t *bias;   // [N] or null
     int *status;
     DqConsts dq;          // dequantiser masks / magics, passed as data (see dequant.cuh)
     int M, N, K, G, ng, log2G;
@@ -66,13 +73,17 @@ struct DecodeParams {
     int wide;        // K % 128 == 0: full stages come in one copy (maps.wide)
     int xpitch;      // bytes per x row in shared memory
     int gmax;        // max groups per CTA slice
+    int silu;        // SiLU-and-multiply epilogue: rows are [gate | up], I = N / 2 each
 };
 
 // Weight tensor maps: `one` loads one 128-k block of RT rows (2-D, exact
 // bounds); `wide` loads NB consecutive blocks in one copy (a 3-D view of the
 // rows as [blocks][row][16 words], only when K is a multiple of 128, so that
 // no block runs past the end of a row).  Fewer, larger copies per stage keep
-// the producer thread's copy issue off the critical path.
+// the producer thread's copy issue off the critical path.  With the SiLU
+// epilogue both views gain a dimension of 2 (gate half, up half, I rows
+// apart) and the boxes are RT / 2 rows high, so one copy still lands RT rows
+// in the same [row][64 B] order.
 struct DecodeMaps {
     CUtensorMap one;
     CUtensorMap wide;
@@ -118,7 +129,10 @@ __global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ 
     const int RT = 16 * R * NW;
     const int rank = (S > 1) ? (int)cg::this_cluster().block_rank() : 0;
     const int tile = blockIdx.x / S;
-    const int n_tile0 = tile * RT;
+    const int silu = p.silu;
+    const int RH = RT / 2;                           // SiLU: gate (and up) rows per CTA
+    const int I = p.N / 2;
+    const int n_tile0 = silu ? tile * RH : tile * RT;
     const int M = p.M, K = p.K, gmax = p.gmax, log2G = p.log2G;
     const DecodeSmem L = decode_layout(R, NW, NB, NS, M, p.xpitch, gmax, ASYM, S);
 
@@ -147,11 +161,18 @@ __global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ 
         const int nbox = min(NB, b1 - bb);
         mbar_arrive_expect_tx(sfull, (uint32_t)nbox * RT * kBoxRowBytes);
         if (p.wide && nbox == NB) {
-            tma_load_3d(sdst, &maps.wide, sfull, 0, n_tile0, bb);
+            if (silu)
+                tma_load_4d(sdst, &maps.wide, sfull, 0, n_tile0, 0, bb);
+            else
+                tma_load_3d(sdst, &maps.wide, sfull, 0, n_tile0, bb);
         } else {
-            for (int j = 0; j < nbox; ++j)
-                tma_load_2d(sdst + (uint32_t)j * RT * kBoxRowBytes, &maps.one, sfull, (bb + j) * (kBoxK / 8),
-                            n_tile0);
+            for (int j = 0; j < nbox; ++j) {
+                const uint32_t d = sdst + (uint32_t)j * RT * kBoxRowBytes;
+                if (silu)
+                    tma_load_3d(d, &maps.one, sfull, (bb + j) * (kBoxK / 8), n_tile0, 0);
+                else
+                    tma_load_2d(d, &maps.one, sfull, (bb + j) * (kBoxK / 8), n_tile0);
+            }
         }
     };
 
@@ -197,8 +218,9 @@ __global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ 
         {
             const int tpr = nthr / RT;
             const int r = (int)threadIdx.x & (RT - 1), gs = (int)threadIdx.x / RT;
-            const int n = n_tile0 + r;
-            const bool vr = n < p.N;
+            // weight row of tile row r (SiLU: gate rows j0.., then up rows I + j0..)
+            const int n = silu ? (r < RH ? n_tile0 + r : I + n_tile0 + (r - RH)) : n_tile0 + r;
+            const bool vr = silu ? (n_tile0 + (r < RH ? r : r - RH) < I) : n < p.N;
             const uint16_t *srow = p.scales + (size_t)(vr ? n : 0) * p.ng + g0;
             const int32_t *zrow = ASYM ? p.qz + (size_t)((vr ? n : 0) >> 3) * p.ng + g0 : nullptr;
             const int zsh = 4 * (n & 7);
@@ -354,25 +376,38 @@ __global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ 
         }
     }
 
-    if (S == 1) {
-        __syncthreads();
-        for (int i = threadIdx.x; i < RT * M; i += blockDim.x) {
-            const int m = i / RT, row = i - (i / RT) * RT;
-            const int n = n_tile0 + row;
-            if (n < p.N) p.out[(size_t)m * p.N + n] = f32_to_dt<DT>(red[row * 8 + m]);
-        }
-    } else if (rank == 0) {
-        // rank 0: own partials (this CTA) and the other ranks' (their bytes
-        // complete the gather barrier), then the sum over ranks in rank order
-        __syncthreads();
-        mbar_wait_cluster_bounded(gbar, 0u, p.status, abort_flag);
-        for (int i = threadIdx.x; i < RT * M; i += blockDim.x) {
-            const int m = i / RT, row = i - (i / RT) * RT;
-            const int n = n_tile0 + row;
-            if (n >= p.N) continue;
-            float sum = red[m * RT + row];
+    // the fp32 sum of tile row `row`, batch column m, over the cluster's ranks
+    // in rank order (S > 1: rank 0's gather buffer [S][M][RT]), plus the bias
+    auto row_sum = [&](int m, int row, int n) -> float {
+        float sum;
+        if (S == 1) {
+            sum = red[row * 8 + m];
+        } else {
+            sum = red[m * RT + row];
             for (int q = 1; q < S; ++q) sum += red[(q * M + m) * RT + row];
-            p.out[(size_t)m * p.N + n] = f32_to_dt<DT>(sum);
+        }
+        if (p.bias != nullptr) sum += dt_to_f32<DT>(p.bias[n]);
+        return sum;
+    };
+    if (S == 1 || rank == 0) {
+        // rank 0 of a cluster: own partials (this CTA) and the other ranks'
+        // (their bytes complete the gather barrier)
+        __syncthreads();
+        if (S > 1) mbar_wait_cluster_bounded(gbar, 0u, p.status, abort_flag);
+        if (!silu) {
+            for (int i = threadIdx.x; i < RT * M; i += blockDim.x) {
+                const int m = i / RT, row = i - (i / RT) * RT;
+                const int n = n_tile0 + row;
+                if (n < p.N) p.out[(size_t)m * p.N + n] = f32_to_dt<DT>(row_sum(m, row, n));
+            }
+        } else {
+            for (int i = threadIdx.x; i < RH * M; i += blockDim.x) {
+                const int m = i / RH, row = i - (i / RH) * RH;
+                const int j = n_tile0 + row;
+                if (j >= I) continue;
+                const float gte = row_sum(m, row, j), up = row_sum(m, RH + row, I + j);
+                p.out[(size_t)m * I + j] = f32_to_dt<DT>(gte / (1.0f + expf(-gte)) * up);
+            }
         }
     }
 }
@@ -412,42 +447,110 @@ bool decode_cfg_valid(const DecodeCfg &c, int M, int K, int G, bool asym) {
     return true;
 }
 
+template <int DT, bool ASYM, int R, int NB>
+static cudaError_t launch_t(const DecodeMaps &tw, const DecodeParams &p, const DecodeCfg &c,
+                            size_t smem, cudaStream_t s, bool pdl, int grid);
+
+// Registers per thread of each kernel instantiation (read once from the
+// compiled kernel), for the residency estimate of the configuration search.
+static int decode_regs(int dtype, bool asym, int R, int NB) {
+    static std::mutex mu;
+    static int cache[2][2][3][3];   // [dtype][asym][R - 1][log2 NB]
+    const int ri = R - 1, ni = NB == 1 ? 0 : (NB == 2 ? 1 : 2);
+    std::lock_guard<std::mutex> lk(mu);
+    int &v = cache[dtype][asym ? 1 : 0][ri][ni];
+    if (v == 0) {
+        const void *f = nullptr;
+#define W4A16_DK(D, A, RR, B) \
+    if (dtype == D && asym == A && R == RR && NB == B) f = reinterpret_cast<const void *>(decode_kernel<D, A, RR, B>);
+        W4A16_DK(0, false, 1, 1) W4A16_DK(0, false, 1, 2) W4A16_DK(0, false, 1, 4)
+        W4A16_DK(0, false, 2, 1) W4A16_DK(0, false, 2, 2) W4A16_DK(0, false, 2, 4)
+        W4A16_DK(0, true, 1, 1) W4A16_DK(0, true, 1, 2) W4A16_DK(0, true, 1, 4)
+        W4A16_DK(0, true, 2, 1) W4A16_DK(0, true, 2, 2) W4A16_DK(0, true, 2, 4)
+        W4A16_DK(1, false, 1, 1) W4A16_DK(1, false, 1, 2) W4A16_DK(1, false, 1, 4)
+        W4A16_DK(1, false, 2, 1) W4A16_DK(1, false, 2, 2) W4A16_DK(1, false, 2, 4)
+        W4A16_DK(1, true, 1, 1) W4A16_DK(1, true, 1, 2) W4A16_DK(1, true, 1, 4)
+        W4A16_DK(1, true, 2, 1) W4A16_DK(1, true, 2, 2) W4A16_DK(1, true, 2, 4)
+#undef W4A16_DK
+        cudaFuncAttributes fa{};
+        if (f == nullptr || cudaFuncGetAttributes(&fa, f) != cudaSuccess) {
+            cudaGetLastError();
+            return 128;                     // conservative; not cached
+        }
+        v = fa.numRegs > 0 ? fa.numRegs : 128;
+    }
+    return v;
+}
+
+// CTAs of configuration c that one SM holds at once: shared memory (plus the
+// 1 KB the runtime reserves per CTA), threads, and registers (allocated per
+// warp in units of 256).
+static long long decode_per_sm(const DecodeCfg &c, int M, int K, int G, bool asym, int dtype, int smem_per_sm) {
+    const long long smem = (long long)decode_smem_bytes(c, M, K, G, asym) + 1024;
+    const int warps = c.NW + 1;
+    const int regs = decode_regs(dtype, asym, c.R, c.NB);
+    const long long warp_regs = ((regs * 32 + 255) / 256) * 256;
+    long long n = smem_per_sm > 0 ? smem_per_sm / smem : 1;
+    n = std::min(n, (long long)(64 / warps));
+    n = std::min(n, 65536LL / (warps * warp_regs));
+    return std::max(n, 0LL);
+}
+
 // Configuration from measured sweeps on GB300 (M = 1 decode, the Qwen3-4B-
 // and Llama-3.1-8B-shaped layers, CUDA graphs with programmatic dependent
 // launch, both per layer and over the four layers of a step in sequence,
 // where a layer's CTAs must leave room for the next layer's to start early;
 // the last search chose each layer's configuration by the time of the whole
-// step, one layer at a time):
-// one 16-row block per warp, 128-k boxes, K split into more cluster CTAs as N
-// shrinks.  The ring is then made as deep as it can be while the whole grid
-// stays resident on the SMs at once (a deeper ring that pushes CTAs into a
-// second wave measured slower than a shallow one).
+// step, one layer at a time): one 16-row block per warp, 128-k boxes, K split
+// into more cluster CTAs as N shrinks.  The whole grid should be resident on
+// the SMs at once (a deeper ring that pushes CTAs into a second wave measured
+// slower than a shallow one; at M >= 3 the staged activations of a long K
+// row alone can do that): from the base choice, the ring is made as deep as
+// it can be while the grid stays in one wave; failing that, fewer boxes per
+// stage and then more cluster CTAs along K are tried, and the configuration
+// with the fewest waves is kept.
 DecodeCfg decode_pick_cfg(int M, int N, int K, int G, int sym, int dtype, int sm_count, int smem_per_sm) {
-    (void)dtype;
-    DecodeCfg c;
+    DecodeCfg b;
     if (N >= 24576)
-        c = DecodeCfg{1, 4, 4, 2, 1};
+        b = DecodeCfg{1, 4, 4, 2, 1};
     else if (N >= 16384)
-        c = DecodeCfg{1, 8, 4, 2, 2};
+        b = DecodeCfg{1, 8, 4, 2, 2};
     else if (N >= 6144)
-        c = K <= 3072 ? DecodeCfg{1, 8, 2, 4, 5} : DecodeCfg{1, 4, 4, 3, 4};
+        b = K <= 3072 ? DecodeCfg{1, 8, 2, 4, 5} : DecodeCfg{1, 4, 4, 3, 4};
     else
-        c = DecodeCfg{1, 4, 4, 4, 8};
+        b = DecodeCfg{1, 4, 4, 4, 8};
+    const bool asym = sym == 0;
     const int nblk = (K + kBoxK - 1) / kBoxK;
-    while (c.S > 1 && nblk / c.S < 1) c.S >>= 1;            // at least one K block per CTA
-    const int nb = (nblk + c.S - 1) / c.S;
-    while (c.NB > 1 && c.NB > nb) c.NB >>= 1;                // 4, 2 or 1 boxes per stage
-    while (!decode_cfg_valid(c, M, K, G, sym == 0) && c.S < 8) c.S *= 2;
-    const int RT = 16 * c.R * c.NW;
-    const long long grid = (long long)((N + RT - 1) / RT) * c.S;
-    for (; c.NS > 2; --c.NS) {
-        if (!decode_cfg_valid(c, M, K, G, sym == 0)) continue;
-        const long long per_cta = (long long)decode_smem_bytes(c, M, K, G, sym == 0) + 1024;
-        long long per_sm = smem_per_sm > 0 ? smem_per_sm / per_cta : 1;
-        per_sm = std::min(per_sm, (long long)(2048 / (32 * (c.NW + 1))));
-        if (grid <= per_sm * sm_count) break;
+    while (b.S > 1 && nblk / b.S < 1) b.S >>= 1;            // at least one K block per CTA
+    const int RT = 16 * b.R * b.NW;
+    const long long tiles = (N + RT - 1) / RT;
+    DecodeCfg best = b;
+    long long best_waves = -1;
+    for (int S = b.S; S <= 8; S *= 2) {
+        if (nblk / S < 1) break;
+        const int nb = (nblk + S - 1) / S;
+        for (int NB = b.NB; NB >= 1; NB >>= 1) {
+            if (NB > nb && NB > 1) continue;                 // 4, 2 or 1 boxes per stage, <= the slice
+            for (int NS = b.NS; NS >= 2; --NS) {
+                DecodeCfg c{b.R, b.NW, NB, NS, S};
+                if (!decode_cfg_valid(c, M, K, G, asym)) continue;
+                const long long per_sm = decode_per_sm(c, M, K, G, asym, dtype, smem_per_sm);
+                if (per_sm <= 0) continue;
+                const long long waves = (tiles * S + per_sm * sm_count - 1) / (per_sm * sm_count);
+                if (waves <= 1) return c;
+                if (best_waves < 0 || waves < best_waves) {
+                    best = c;
+                    best_waves = waves;
+                }
+            }
+        }
+        if (S == 8) break;
     }
-    return c;
+    if (best_waves < 0) {                                    // nothing valid: the smallest footprint
+        best = DecodeCfg{b.R, b.NW, 1, 2, b.S};
+        while (!decode_cfg_valid(best, M, K, G, asym) && best.S < 8) best.S *= 2;
+    }
+    return best;
 }
 
 template <int DT, bool ASYM, int R, int NB>
@@ -518,22 +621,31 @@ cudaError_t launch_decode(const GemmArgs &a, const DecodeCfg &c, const DeviceInf
     const bool wide = a.K % kBoxK == 0;
     {
         EncodeTiledFn encode = reinterpret_cast<EncodeTiledFn>(dev.encode_tiled);
-        cuuint64_t dims[2] = {(cuuint64_t)(a.K / 8), (cuuint64_t)a.N};
-        cuuint64_t strides[1] = {(cuuint64_t)(a.K / 8) * 4};
-        cuuint32_t box[2] = {(cuuint32_t)(kBoxK / 8), (cuuint32_t)RT};
-        cuuint32_t estr[2] = {1, 1};
-        CUresult r = encode(&tw.one, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<int32_t *>(a.qweight), dims,
-                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+        // rows as [N] or, with SiLU, as [2][I] (a dimension of 2 with stride I rows)
+        const int silu = a.silu_mul ? 1 : 0;
+        const cuuint64_t rows = silu ? (cuuint64_t)(a.N / 2) : (cuuint64_t)a.N;
+        const cuuint64_t row_bytes = (cuuint64_t)(a.K / 8) * 4;
+        const cuuint32_t box_rows = silu ? (cuuint32_t)(RT / 2) : (cuuint32_t)RT;
+        cuuint64_t dims[3] = {(cuuint64_t)(a.K / 8), rows, 2};
+        cuuint64_t strides[2] = {row_bytes, row_bytes * rows};
+        cuuint32_t box[3] = {(cuuint32_t)(kBoxK / 8), box_rows, 2};
+        cuuint32_t estr[4] = {1, 1, 1, 1};
+        CUresult r = encode(&tw.one, CU_TENSOR_MAP_DATA_TYPE_INT32, 2 + silu, const_cast<int32_t *>(a.qweight),
+                            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
         tw.wide = tw.one;
         if (wide) {
-            cuuint64_t dims3[3] = {(cuuint64_t)(kBoxK / 8), (cuuint64_t)a.N, (cuuint64_t)(a.K / kBoxK)};
-            cuuint64_t strides3[2] = {(cuuint64_t)(a.K / 8) * 4, (cuuint64_t)kBoxRowBytes};
-            cuuint32_t box3[3] = {(cuuint32_t)(kBoxK / 8), (cuuint32_t)RT, (cuuint32_t)c.NB};
-            cuuint32_t estr3[3] = {1, 1, 1};
-            r = encode(&tw.wide, CU_TENSOR_MAP_DATA_TYPE_INT32, 3, const_cast<int32_t *>(a.qweight), dims3,
-                       strides3, box3, estr3, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            // [blocks][(half)][row][16 words]
+            cuuint64_t dw[4], sw[3];
+            cuuint32_t bw[4];
+            int nd = 0;
+            dw[nd] = kBoxK / 8; bw[nd++] = kBoxK / 8;
+            dw[nd] = rows; bw[nd] = box_rows; sw[nd - 1] = row_bytes; ++nd;
+            if (silu) { dw[nd] = 2; bw[nd] = 2; sw[nd - 1] = row_bytes * rows; ++nd; }
+            dw[nd] = (cuuint64_t)(a.K / kBoxK); bw[nd] = (cuuint32_t)c.NB; sw[nd - 1] = kBoxRowBytes; ++nd;
+            r = encode(&tw.wide, CU_TENSOR_MAP_DATA_TYPE_INT32, nd, const_cast<int32_t *>(a.qweight), dw, sw, bw,
+                       estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
             if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
         }
@@ -543,6 +655,8 @@ cudaError_t launch_decode(const GemmArgs &a, const DecodeCfg &c, const DeviceInf
     p.scales = (const uint16_t *)a.scales;
     p.qz = a.qzeros;
     p.out = (uint16_t *)a.out;
+    p.bias = (const uint16_t *)a.bias;
+    p.silu = a.silu_mul ? 1 : 0;
     p.status = dev.status;
     p.dq = dq_consts_i4(a.dtype);
     p.M = a.M;
@@ -559,7 +673,7 @@ cudaError_t launch_decode(const GemmArgs &a, const DecodeCfg &c, const DeviceInf
     p.wide = wide ? 1 : 0;
     p.xpitch = decode_xpitch(c, a.K);
     p.gmax = decode_gmax(c, a.K, a.G);
-    const int tiles = (a.N + RT - 1) / RT;
+    const int tiles = a.silu_mul ? (a.N / 2 + RT / 2 - 1) / (RT / 2) : (a.N + RT - 1) / RT;
     const int grid = tiles * c.S;
     const size_t smem = decode_smem_bytes(c, a.M, a.K, a.G, asym);
     return launch_dispatch(a.dtype, asym, c.R, c.NB, tw, p, c, smem, s, pdl, grid);

@@ -14,6 +14,8 @@ struct GemmArgs {
     void *out;
     int M, N, K, G;
     int dtype;              // 0 fp16, 1 bf16
+    const void *bias = nullptr;  // [N] in the activation dtype, or none
+    int silu_mul = 0;       // 1: out [M, N/2] = silu(y[:, :N/2]) * y[:, N/2:] (rows 0..N/2-1 = gate)
 };
 
 // Per-device facts the launchers need.

@@ -26,8 +26,9 @@
 //    vector load per tile, issued after the tile's first arrive (an arrive
 //    has release semantics and would otherwise wait for the loads to land).
 //    After the main loop the same warps are the epilogue:
-//    tcgen05.ld from TMEM (lane quadrant = warp % 4), one rounding to the
-//    output dtype, a [BN x 256] tile staged in shared memory, one TMA store.
+//    tcgen05.ld from TMEM (lane quadrant = warp % 4), the optional bias of
+//    the row added, one rounding to the output dtype, a [BN x 256] tile
+//    staged in shared memory, one TMA store.
 //  * Warp 1: TMEM allocation (512 columns: two fp32 accumulators) and the
 //    single-thread MMA issuer (tcgen05.mma.cta_group::1.kind::f16,
 //    128 x BN x 16 per instruction, two per 16 k); tcgen05.commit releases
@@ -68,6 +69,7 @@ struct PrefillParams {
     const uint16_t *scales;
     const int32_t *qz;
     uint16_t *out;        // y [M, N] (written directly when K is split; else by TMA store)
+    const uint16_t *bias; // [N] added before the rounding, or null
     int M, N, K, G, ng;
     int BN, SX, SA, SW;
     int n_mtiles;
@@ -84,6 +86,12 @@ __device__ __forceinline__ uint16_t f32_to_dt16(float v) {
         __nv_bfloat16 h = __float2bfloat16_rn(v);
         return *reinterpret_cast<uint16_t *>(&h);
     }
+}
+
+template <int DT>
+__device__ __forceinline__ float dt16_to_f32(uint16_t v) {
+    if (DT == 0) return __half2float(__ushort_as_half(v));
+    return __bfloat162float(__ushort_as_bfloat16(v));
 }
 
 struct SmemLayout {
@@ -402,12 +410,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int nl = h * kHalf + 32 * q + lane;            // row of the tile
                 const uint32_t tbase = tmem_d + ((uint32_t)(32 * q) << 16) + (uint32_t)(h * 256);
                 uint16_t *stage = reinterpret_cast<uint16_t *>(smem);   // [BN][256], over x/A rings
+                const float bv = (p.bias != nullptr && n0 + nl < p.N) ? dt16_to_f32<DT>(p.bias[n0 + nl]) : 0.f;
                 for (int c0 = 0; c0 < p.BN; c0 += 16) {
                     uint32_t v[16];
                     tmem_ld_32x32b_x16(tbase + (uint32_t)c0, v);
 #pragma unroll
                     for (int jx = 0; jx < 16; ++jx)
-                        stage[(size_t)(c0 + jx) * kBW + nl] = f32_to_dt16<DT>(__uint_as_float(v[jx]));
+                        stage[(size_t)(c0 + jx) * kBW + nl] = f32_to_dt16<DT>(__uint_as_float(v[jx]) + bv);
                 }
                 fence_proxy_async_smem();
             }
@@ -445,6 +454,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float4 t = *reinterpret_cast<const float4 *>(peer[q] + off);
                     sum.x += t.x; sum.y += t.y; sum.z += t.z; sum.w += t.w;
                 }
+            }
+            if (p.bias != nullptr) {
+                sum.x += dt16_to_f32<DT>(p.bias[n]);
+                if (n + 1 < p.N) sum.y += dt16_to_f32<DT>(p.bias[n + 1]);
+                if (n + 2 < p.N) sum.z += dt16_to_f32<DT>(p.bias[n + 2]);
+                if (n + 3 < p.N) sum.w += dt16_to_f32<DT>(p.bias[n + 3]);
             }
             const uint16_t o0 = f32_to_dt16<DT>(sum.x), o1 = f32_to_dt16<DT>(sum.y);
             const uint16_t o2 = f32_to_dt16<DT>(sum.z), o3 = f32_to_dt16<DT>(sum.w);
@@ -673,6 +688,7 @@ cudaError_t launch_prefill(const GemmArgs &a, const PrefillCfg &c, const DeviceI
     p.scales = (const uint16_t *)a.scales;
     p.qz = a.qzeros;
     p.out = (uint16_t *)a.out;
+    p.bias = (const uint16_t *)a.bias;
     p.M = a.M;
     p.N = a.N;
     p.K = a.K;

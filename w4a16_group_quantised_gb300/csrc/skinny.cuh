@@ -81,6 +81,12 @@ __device__ __forceinline__ uint16_t f32_to_dt(float v) {
     return *reinterpret_cast<uint16_t *>(&h);
 }
 
+template <int DT>
+__device__ __forceinline__ float dt_to_f32(uint16_t v) {
+    if (DT == 0) return __half2float(__ushort_as_half(v));
+    return __bfloat162float(__ushort_as_bfloat16(v));
+}
+
 // Plain C++ loads from the dynamic shared-memory block (the compiler
 // schedules them freely between the barrier waits, which carry memory
 // clobbers).  The kernels derive their aligned base by pointer arithmetic on
