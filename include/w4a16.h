@@ -43,6 +43,11 @@
  * it and the GEMM, or early start switched off (environment W4A16_PDL=0 or
  * w4a16_debug_set_config(3, {0}, 1)).
  *
+ * Kernel-selection log: with the environment variable W4A16_LOG=1 (read on
+ * the first call on a device) each GEMM entry point prints the kernel it
+ * launched -- path, kernel, its configuration, grid, early start, epilogue
+ * -- to stderr, each distinct line once; W4A16_LOG=2 prints every call.
+ *
  * Errors: arguments are validated on the host before anything is launched;
  * an invalid call returns a negative w4a16_status_t and launches nothing.
  * M == 0 (or N == 0 for pack) is a valid no-op.  A launch failure returns
@@ -273,6 +278,11 @@ int w4a16_version(void);
  * which = 3: programmatic dependent launch on/off, vals = {flag}, n = 1;
  * which = 4: balanced decode kernel vals = {on (1) / off (0), load ring
  * depth in units (2, 4 or 6)}, n = 2;
+ * which = 7: test of the timeout path, vals = {on (1) / off (0)}, n = 1:
+ * while on, the decode kernel issues no weight copies, so every CTA's bounded
+ * wait for them runs out (about 2 s), the kernel leaves without touching
+ * memory beyond its own output and records W4A16_ERR_TIMEOUT in the status
+ * word (its output is then meaningless); n = 0 turns it off;
  * n = 0 restores the built-in choice for which = 1, 2 or 4.  An invalid
  * configuration is rejected here or, for the decode shape limits, by the
  * next w4a16_gemm call with W4A16_ERR_ARG. */

@@ -138,6 +138,9 @@ def test_debug_config_validation(lib):
     assert lib.w4a16_debug_set_config(9, None, 0) == -9
     assert lib.w4a16_debug_set_config(5, None, 0) == -9   # no such hook
     assert lib.w4a16_debug_set_config(6, None, 0) == -9
+    assert lib.w4a16_debug_set_config(7, None, 0) == 0    # timeout-path test hook off
+    arr = (ctypes.c_int * 2)(1, 1)
+    assert lib.w4a16_debug_set_config(7, arr, 2) == -9
 
 
 def test_fused_entry_point_limits(lib):

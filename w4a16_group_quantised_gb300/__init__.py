@@ -16,6 +16,7 @@ from .binding import (  # noqa: F401
     W4A16Error,
     library_path,
     load_library,
+    w4a16_clear_device_error,
     w4a16_debug_set_config,
     w4a16_dequant_debug,
     w4a16_gemm,

@@ -323,7 +323,9 @@ def w4a16_debug_set_config(which: int, vals=None) -> None:
     """Tuning hook (see include/w4a16.h): which=1 cluster decode kernel
     {R, NW, NB, NS, S}; which=2 prefill {BN, x stages, A stages, W stages[, KS]};
     which=3 programmatic dependent launch {flag}; which=4 balanced decode
-    kernel {on, ring depth}.  vals=None restores the built-in choice."""
+    kernel {on, ring depth}; which=7 timeout-path test {on} (decode kernels
+    issue no weight copies, so their bounded waits run out).  vals=None
+    restores the built-in choice."""
     lib = load_library()
     if vals is None:
         rc = lib.w4a16_debug_set_config(which, None, 0)
@@ -336,3 +338,9 @@ def w4a16_debug_set_config(which: int, vals=None) -> None:
 def w4a16_last_device_error() -> int:
     """Status word written by kernels whose bounded waits ran out (0 = none)."""
     return load_library().w4a16_last_device_error()
+
+
+def w4a16_clear_device_error() -> None:
+    """Synchronise the device and reset the status word (and the balanced
+    decode kernel's tickets) after a timeout."""
+    _check("w4a16_clear_device_error", load_library().w4a16_clear_device_error())

@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <functional>
@@ -54,8 +55,34 @@ DecodeCfg g_decode_cfg{};
 bool g_prefill_override = false;
 PrefillCfg g_prefill_cfg{};
 int g_pdl = 1;
+// Kernel-selection log to stderr (environment W4A16_LOG): 0 off, 1 each
+// distinct selection once, 2 every call.
+int g_log = 0;
+std::mutex g_log_mu;
+uint64_t g_log_seen[512];
+int g_n_log_seen = 0;
+
+void log_selection(const char *line) {
+    int mode;
+    {
+        std::lock_guard<std::mutex> lk(g_cfg_mu);
+        mode = g_log;
+    }
+    if (mode <= 0) return;
+    std::lock_guard<std::mutex> lk(g_log_mu);
+    if (mode == 1) {
+        uint64_t h = 1469598103934665603ull;              // FNV-1a of the line
+        for (const char *c = line; *c; ++c) h = (h ^ (unsigned char)*c) * 1099511628211ull;
+        for (int i = 0; i < g_n_log_seen; ++i)
+            if (g_log_seen[i] == h) return;
+        if (g_n_log_seen < 512) g_log_seen[g_n_log_seen++] = h;
+    }
+    std::fprintf(stderr, "w4a16: %s\n", line);
+}
 // balanced decode kernel: enabled flag and preferred ring depth
 int g_sk_on = 0, g_sk_ns = 4;
+// test hook (w4a16_debug_set_config(7)): decode kernels issue no weight copies
+int g_hold_copies = 0;
 // Streams whose last library launch wrote weights (w4a16_pack,
 // w4a16_pack_zeros): the next GEMM on such a stream is launched without
 // programmatic dependent launch, because the GEMM kernels read weights
@@ -123,7 +150,12 @@ void init_device(DevState &st, int dev) {
         return;
     }
     const char *e = std::getenv("W4A16_PDL");
-    if (e && e[0] == '0') g_pdl = 0;
+    const char *lg = std::getenv("W4A16_LOG");
+    {
+        std::lock_guard<std::mutex> lk(g_cfg_mu);
+        if (e && e[0] == '0') g_pdl = 0;
+        if (lg) g_log = std::atoi(lg);
+    }
     st.rc = W4A16_OK;
 }
 
@@ -259,10 +291,11 @@ int run_gemm(const void *x, int M, int K, const int32_t *qw, const void *scales,
     cudaError_t e;
     if (path == W4A16_PATH_DECODE) {
         int sk_on, ns_pref;
-        bool cluster_override;
+        bool cluster_override, hold;
         DecodeCfg c;
         {
             std::lock_guard<std::mutex> lk(g_cfg_mu);
+            hold = g_hold_copies != 0;
             sk_on = g_sk_on && !g_decode_override;
             ns_pref = g_sk_ns;
             cluster_override = g_decode_override;
@@ -270,15 +303,31 @@ int run_gemm(const void *x, int M, int K, const int32_t *qw, const void *scales,
         }
         float *ws = nullptr;
         int *cnt = nullptr;
-        if (plain && sk_on && (N + 15) / 16 <= kDecodeTickets && decode_sk_applicable(M, K) &&
+        if (plain && !hold && sk_on && (N + 15) / 16 <= kDecodeTickets && decode_sk_applicable(M, K) &&
             stream_scratch(*st, s, &ws, &cnt)) {
             e = launch_decode_sk(a, ns_pref, *dev, ws, cnt, s, pdl);
+            char line[256];
+            std::snprintf(line, sizeof line, "gemm M=%d N=%d K=%d G=%d %s %s path=decode kernel=decode_sk ring=%d pdl=%d",
+                          M, N, K, G, dtype == 0 ? "fp16" : "bf16", asym ? "asym" : "sym", ns_pref, pdl ? 1 : 0);
+            log_selection(line);
             return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
         }
         if (!cluster_override)
             c = decode_pick_cfg(M, N, K, G, qz == nullptr, dtype, dev->sm_count, dev->smem_per_sm);
         if (!decode_cfg_valid(c, M, K, G, asym)) return W4A16_ERR_ARG;
-        e = launch_decode(a, c, *dev, s, pdl);
+        e = launch_decode(a, c, *dev, s, pdl, hold);
+        {
+            const int RT = 16 * c.R * c.NW;
+            const int tiles = a.silu_mul ? (N / 2 + RT / 2 - 1) / (RT / 2) : (N + RT - 1) / RT;
+            char line[320];
+            std::snprintf(line, sizeof line,
+                          "gemm M=%d N=%d K=%d G=%d %s %s path=decode kernel=decode_kernel R=%d NW=%d NB=%d NS=%d "
+                          "S=%d grid=%d pdl=%d bias=%d epilogue=%s%s",
+                          M, N, K, G, dtype == 0 ? "fp16" : "bf16", asym ? "asym" : "sym", c.R, c.NW, c.NB, c.NS,
+                          c.S, tiles * c.S, pdl ? 1 : 0, bias != nullptr ? 1 : 0,
+                          a.silu_mul ? "silu_mul" : "none", cluster_override ? " (forced)" : "");
+            log_selection(line);
+        }
     } else {
         PrefillCfg c;
         {
@@ -287,6 +336,13 @@ int run_gemm(const void *x, int M, int K, const int32_t *qw, const void *scales,
                                    : prefill_pick_cfg(M, N, K, G, qz == nullptr, dtype, *dev);
         }
         e = launch_prefill(a, c, *dev, s, pdl);
+        char line[320];
+        std::snprintf(line, sizeof line,
+                      "gemm M=%d N=%d K=%d G=%d %s %s path=prefill kernel=prefill_kernel BN=%d x_stages=%d "
+                      "a_stages=%d w_stages=%d ks=%d pdl=%d bias=%d",
+                      M, N, K, G, dtype == 0 ? "fp16" : "bf16", asym ? "asym" : "sym", c.BN, c.stages, c.astages,
+                      c.wstages, c.ks, pdl ? 1 : 0, bias != nullptr ? 1 : 0);
+        log_selection(line);
     }
     return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
 }
@@ -514,6 +570,12 @@ int w4a16_debug_set_config(int which, const int *vals, int n) {
     if (which == 3) {
         if (n != 1 || vals == nullptr) return W4A16_ERR_ARG;
         g_pdl = vals[0] != 0;
+        return W4A16_OK;
+    }
+    if (which == 7) {
+        if (n == 0) { g_hold_copies = 0; return W4A16_OK; }
+        if (n != 1 || vals == nullptr) return W4A16_ERR_ARG;
+        g_hold_copies = vals[0] != 0;
         return W4A16_OK;
     }
     if (which == 4) {

@@ -74,6 +74,7 @@ struct DecodeParams {
     int xpitch;      // bytes per x row in shared memory
     int gmax;        // max groups per CTA slice
     int silu;        // SiLU-and-multiply epilogue: rows are [gate | up], I = N / 2 each
+    int hold;        // test hook: issue no weight copies, so the bounded waits run out
 };
 
 // Weight tensor maps: `one` loads one 128-k block of RT rows (2-D, exact
@@ -194,7 +195,7 @@ __global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ 
         // ------------------------------------------------------------ producer
         // Step st refills slot st % NS once the compute warps have released
         // step st - NS from it.
-        if (lane == 0) {
+        if (lane == 0 && !p.hold) {
             tma_prefetch_desc(&maps.one);
             if (p.wide) tma_prefetch_desc(&maps.wide);
             for (int st = 0; st < nsteps; ++st) {
@@ -613,7 +614,7 @@ static cudaError_t launch_dispatch(int dtype, bool asym, int R, int NB, const De
 }
 
 cudaError_t launch_decode(const GemmArgs &a, const DecodeCfg &c, const DeviceInfo &dev,
-                          cudaStream_t s, bool pdl) {
+                          cudaStream_t s, bool pdl, bool hold_copies) {
     if (dev.encode_tiled == nullptr) return cudaErrorNotSupported;
     const bool asym = a.qzeros != nullptr;
     const int RT = 16 * c.R * c.NW;
@@ -657,6 +658,7 @@ cudaError_t launch_decode(const GemmArgs &a, const DecodeCfg &c, const DeviceInf
     p.out = (uint16_t *)a.out;
     p.bias = (const uint16_t *)a.bias;
     p.silu = a.silu_mul ? 1 : 0;
+    p.hold = hold_copies ? 1 : 0;
     p.status = dev.status;
     p.dq = dq_consts_i4(a.dtype);
     p.M = a.M;

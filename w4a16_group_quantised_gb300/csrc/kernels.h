@@ -46,8 +46,10 @@ struct DecodeCfg {
 DecodeCfg decode_pick_cfg(int M, int N, int K, int G, int sym, int dtype, int sm_count, int smem_per_sm);
 bool decode_cfg_valid(const DecodeCfg &c, int M, int K, int G, bool asym);
 size_t decode_smem_bytes(const DecodeCfg &c, int M, int K, int G, bool asym);
+// hold_copies: test hook -- the kernel issues no weight copies, so its bounded
+// waits run out and it exits with W4A16_ERR_TIMEOUT in the status word.
 cudaError_t launch_decode(const GemmArgs &a, const DecodeCfg &c, const DeviceInfo &dev,
-                          cudaStream_t s, bool pdl);
+                          cudaStream_t s, bool pdl, bool hold_copies = false);
 
 // Per-stream scratch of the balanced decode kernel: kDecodeTickets ints
 // (zero between calls) and decode_sk_workspace_floats(sm_count) floats.
