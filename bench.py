@@ -379,6 +379,40 @@ def bench_prefill(w, steps, reps=5):
                 per_shape_tflops=[f / t / 1e12 for f, t in zip(flops, per_s)])
 
 
+def bench_prefill_cache(w, M, steps, reps=5):
+    """The Llama-3.1-8B-shaped layers at M through the dequantised prefill
+    cache (w4a16_gemm_dense on W = RN((q - z) s) built once by
+    w4a16_dequantize, not timed): per-shape and whole-step medians."""
+    shapes = wl.LLAMA31_8B_SHAPES
+    layers = [upload(w, wl.llama31_8b_prefill(i, M)) for i in range(len(shapes))]
+    caches = [w.w4a16_dequantize(d["qweight"], d["scales"], d["qzeros"], d["G"]) for d in layers]
+    outs = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for (_, N, K) in shapes]
+    flops = [2 * M * N * K for (_, N, K) in shapes]
+    stream = torch.cuda.Stream()
+
+    def region(only):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            for i, (d, c, o) in enumerate(zip(layers, caches, outs)):
+                if only is None or i == only:
+                    w.w4a16_gemm_dense(d["x"], c, out=o)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1000.0 / steps
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            region(None)
+        per_s = [statistics.median(region(i) for _ in range(reps)) for i in range(len(shapes))]
+        dt = statistics.median(region(None) for _ in range(reps))
+    del layers, caches, outs
+    torch.cuda.empty_cache()
+    return dict(tflops=sum(flops) / dt / 1e12, ms_per_step=dt * 1e3,
+                per_shape_tflops={n: round(f / t / 1e12, 1) for (n, _, _), f, t in zip(shapes, flops, per_s)},
+                per_shape_us={n: round(t * 1e6, 2) for (n, _, _), t in zip(shapes, per_s)})
+
+
 def profile_case(w, which, steps, warmup, m=None):
     """A short run for ncu captures: `warmup` then `steps` eager passes over
     the four layers of one workload (one set of inputs, launched in layer
@@ -653,6 +687,13 @@ def main():
             r["per_shape"][name]["TFLOP/s"] = round(2 * 128 * N * K / (r["per_shape"][name]["us"] * 1e-6) / 1e12, 1)
         r["TFLOP/s"] = round(sum(2 * 128 * N * K for (_, N, K) in lshapes) / (r["step_us"] * 1e-6) / 1e12, 1)
         extra["prefill_llama31_8b_m128"] = dict(workload="llama-3.1-8b-prefill-m128-asym-g64-bf16", **r)
+        for Mc in (1920, 128):
+            rc = bench_prefill_cache(w, Mc, max(2, args.prefill_steps))
+            extra[f"prefill_dense_cache_m{Mc}"] = dict(
+                workload=f"llama-3.1-8b-prefill-m{Mc}-bf16, dequantised weight cache (w4a16_gemm_dense)",
+                value=round(rc["tflops"], 2), unit="TFLOP/s", ms_per_step=round(rc["ms_per_step"], 4),
+                per_shape_tflops=rc["per_shape_tflops"], per_shape_us=rc["per_shape_us"],
+                frac_of_burst=round(rc["tflops"] / tc, 4))
 
     pre = bench_prefill(w, max(2, args.prefill_steps))
     dom = int(np.argmax(pre["per_shape_ms"]))

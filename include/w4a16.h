@@ -191,6 +191,36 @@ int w4a16_gemm_fused(const void *x, int M, int K, const int32_t *qweight, const 
                      int epilogue, void *out, w4a16_stream_t stream, w4a16_dtype_t dtype,
                      w4a16_path_t path);
 
+/* Dequantised prefill cache.  Source: "[ROCm] Converge the two W4A16 linear
+ * kernels onto the upstream shell", section "What this does": an optional
+ * dequantised copy of the weight that prefill reads with a plain dtype GEMM,
+ * while decode keeps reading the int4 weight.
+ *
+ * w4a16_dequantize: w_out [N, K] (natural order, `dtype`, 16-byte aligned,
+ * caller-owned; N * K * 2 bytes) = RN_dtype((q - z) * s) -- the values
+ * w4a16_dequant_debug writes, here as the product entry point that builds the
+ * cache.  Arguments and errors as w4a16_dequant_debug. */
+int w4a16_dequantize(const int32_t *qweight, const void *scales, const int32_t *qzeros_or_null,
+                     int G, int N, int K, void *w_out, w4a16_dtype_t dtype, w4a16_stream_t stream);
+
+/* out [M, N] = RN(x . W^T (+ bias)) for a dense weight W [N, K] in `dtype`
+ * (e.g. from w4a16_dequantize): the prefill kernel with its weight operand
+ * loaded directly into shared memory by TMA (no dequantisation), fp32
+ * accumulation in tensor memory.  Requires M >= 0, N > 0 and K > 0 both
+ * multiples of 8, x, w, out 16-byte aligned, bias (optional, [N]) 2-byte
+ * aligned.  Errors as w4a16_gemm. */
+int w4a16_gemm_dense(const void *x, int M, int K, const void *w, int N, const void *bias_or_null,
+                     void *out, w4a16_dtype_t dtype, w4a16_stream_t stream);
+
+/* w4a16_gemm with an optional prefill cache: when w_cache_or_null is given
+ * and the dispatcher routes M to the prefill path, the call runs
+ * w4a16_gemm_dense on the cache; otherwise (decode-sized M, or no cache) it
+ * is w4a16_gemm on the int4 weight.  Both give RN((q - z) s)-weight results
+ * within the same tolerance (the cache holds exactly those weights). */
+int w4a16_gemm_cached(const void *x, int M, int K, const int32_t *qweight, const void *scales,
+                      const int32_t *qzeros_or_null, int G, int N, const void *w_cache_or_null,
+                      void *out, w4a16_stream_t stream, w4a16_dtype_t dtype);
+
 /* One layer of a chain (w4a16_gemm_chain): its weights, optional bias,
  * epilogue and output buffer.  N, K and G as in w4a16_gemm. */
 typedef struct {

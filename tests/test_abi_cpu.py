@@ -244,3 +244,25 @@ def test_chain_entry_point_limits(lib):
     assert f(ALIGNED, 1, None, 2, 0, None) == -1
     assert f(ALIGNED, 1, None, 0, 0, None) == 0
     assert f(ALIGNED, 1, None, -1, 0, None) == -9
+
+
+def test_cache_entry_point_limits(lib):
+    """w4a16_gemm_dense / w4a16_dequantize / w4a16_gemm_cached validate on the host."""
+    f = lib.w4a16_gemm_dense
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+    assert f(ALIGNED, 1, 100, ALIGNED, 64, None, ALIGNED, 0, None) == -2      # K % 8
+    assert f(ALIGNED, 1, 128, ALIGNED, 60, None, ALIGNED, 0, None) == -2      # N % 8
+    assert f(ALIGNED, 1, 128, NULL, 64, None, ALIGNED, 0, None) == -1
+    assert f(MISALIGNED, 1, 128, ALIGNED, 64, None, ALIGNED, 0, None) == -4
+    assert f(ALIGNED, 1, 128, ALIGNED, 64, ODD, ALIGNED, 0, None) == -4
+    assert f(ALIGNED, 1, 128, ALIGNED, 64, None, ALIGNED, 5, None) == -5
+    assert f(None, 0, 128, ALIGNED, 64, None, None, 0, None) == 0             # M == 0
+    g = lib.w4a16_dequantize
+    g.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 + [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+    assert g(ALIGNED, ALIGNED, None, 40, 64, 160, ALIGNED, 0, None) == -3
+    h = lib.w4a16_gemm_cached
+    h.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int] + [ctypes.c_void_p] * 3 + [ctypes.c_int] * 2 + \
+        [ctypes.c_void_p] * 3 + [ctypes.c_int]
+    assert h(ALIGNED, 1, 128, ALIGNED, ALIGNED, None, 48, 64, ALIGNED, ALIGNED, None, 0) == -3
+    assert h(None, 0, 128, ALIGNED, ALIGNED, None, 32, 64, ALIGNED, None, None, 0) == 0

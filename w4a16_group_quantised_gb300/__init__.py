@@ -20,7 +20,10 @@ from .binding import (  # noqa: F401
     w4a16_debug_set_config,
     w4a16_dequant_debug,
     w4a16_gemm,
+    w4a16_dequantize,
+    w4a16_gemm_cached,
     w4a16_gemm_chain,
+    w4a16_gemm_dense,
     w4a16_gemm_decode_noalloc,
     w4a16_gemm_fused,
     w4a16_gemm_host,

@@ -60,6 +60,9 @@ def load_library():
             "w4a16_gemm_ex": [P, I, I, P, P, P, I, I, P, P, I, I],
             "w4a16_gemm_fused": [P, I, I, P, P, P, I, I, P, I, P, P, I, I],
             "w4a16_gemm_chain": [P, I, P, I, I, P],
+            "w4a16_dequantize": [P, P, P, I, I, I, P, I, P],
+            "w4a16_gemm_dense": [P, I, I, P, I, P, P, I, P],
+            "w4a16_gemm_cached": [P, I, I, P, P, P, I, I, P, P, P, I],
             "w4a16_gemm_host": [P, I, I, P, P, P, I, I, P, I, P, P, P],
             "w4a16_gemm_decode_noalloc": [P, I, I, P, P, P, I, I, P, P, I],
             "w4a16_select_path": [I, I, I, I, I, I],
@@ -243,6 +246,62 @@ def w4a16_gemm_fused(x, qweight, scales, qzeros, G: int, bias=None, epilogue: in
     rc = lib.w4a16_gemm_fused(_p(x), M, K, _p(qweight), _p(scales), _p(qzeros), G, N, _p(bias), epilogue,
                               _p(out), _stream_ptr(stream), dt, path)
     _check("w4a16_gemm_fused", rc)
+    return out
+
+
+def w4a16_dequantize(qweight, scales, qzeros, G: int, out=None, stream=None):
+    """The dequantised prefill cache: W [N, K] = RN_dtype((q - z) * s) in the
+    scales' dtype (natural order)."""
+    import torch
+    _require_int32("qweight", qweight)
+    _require_int32("qzeros", qzeros)
+    N, K8 = qweight.shape
+    K = K8 * 8
+    if out is None:
+        out = torch.empty((N, K), dtype=scales.dtype, device=qweight.device)
+    rc = load_library().w4a16_dequantize(_p(qweight), _p(scales), _p(qzeros), G, N, K, _p(out),
+                                         _dtype_code(scales), _stream_ptr(stream))
+    _check("w4a16_dequantize", rc)
+    return out
+
+
+def w4a16_gemm_dense(x, w, bias=None, out=None, stream=None):
+    """out [M, N] = x . W^T (+ bias) for a dense weight W [N, K] of x's dtype."""
+    import torch
+    for name, t in (("x", x), ("w", w), ("bias", bias), ("out", out)):
+        if t is not None and (not isinstance(t, torch.Tensor) or t.device.type != "cuda" or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    dt = _dtype_code(x)
+    if w.dtype != x.dtype or (bias is not None and bias.dtype != x.dtype):
+        raise TypeError("w and bias must have the dtype of x")
+    M, K = x.shape
+    N = w.shape[0]
+    if w.dim() != 2 or w.shape[1] != K:
+        raise ValueError(f"w must be [N, {K}], got {list(w.shape)}")
+    if bias is not None and list(bias.shape) != [N]:
+        raise ValueError(f"bias must be [{N}]")
+    if out is None:
+        out = torch.empty((M, N), dtype=x.dtype, device=x.device)
+    elif list(out.shape) != [M, N] or out.dtype != x.dtype:
+        raise ValueError(f"out must be [{M}, {N}] of x's dtype")
+    rc = load_library().w4a16_gemm_dense(_p(x), M, K, _p(w), N, _p(bias), _p(out), dt, _stream_ptr(stream))
+    _check("w4a16_gemm_dense", rc)
+    return out
+
+
+def w4a16_gemm_cached(x, qweight, scales, qzeros, G: int, w_cache=None, out=None, stream=None):
+    """w4a16_gemm, except that prefill-sized M reads the dequantised cache
+    w_cache [N, K] (if given) through w4a16_gemm_dense."""
+    import torch
+    M, K, N = _check_gemm_operands(x, qweight, scales, qzeros, G, out)
+    if w_cache is not None and (w_cache.dtype != x.dtype or list(w_cache.shape) != [N, K]
+                                or not w_cache.is_contiguous() or w_cache.device != x.device):
+        raise ValueError(f"w_cache must be a contiguous [{N}, {K}] tensor of x's dtype on x's device")
+    if out is None:
+        out = torch.empty((M, N), dtype=x.dtype, device=x.device)
+    rc = load_library().w4a16_gemm_cached(_p(x), M, K, _p(qweight), _p(scales), _p(qzeros), G, N, _p(w_cache),
+                                          _p(out), _stream_ptr(stream), _dtype_code(x))
+    _check("w4a16_gemm_cached", rc)
     return out
 
 

@@ -462,6 +462,71 @@ int w4a16_gemm_fused(const void *x, int M, int K, const int32_t *qweight, const 
                     bias_or_null, epilogue);
 }
 
+int w4a16_dequantize(const int32_t *qweight, const void *scales, const int32_t *qzeros_or_null, int G, int N,
+                     int K, void *w_out, w4a16_dtype_t dtype, w4a16_stream_t stream) {
+    return w4a16_dequant_debug_ex(qweight, scales, qzeros_or_null, G, N, K, w_out, dtype, stream, W4A16_DQ_PREFILL);
+}
+
+namespace {
+int run_gemm_dense(const void *x, int M, int K, const void *w, int N, const void *bias, void *out, int dtype,
+                   w4a16_stream_t stream) {
+    if (dtype != W4A16_F16 && dtype != W4A16_BF16) return W4A16_ERR_DTYPE;
+    if (M < 0 || N <= 0 || K <= 0 || N % 8 != 0 || K % 8 != 0) return W4A16_ERR_SHAPE;
+    if ((long long)M * K >= (1LL << 31) || (long long)N * K >= (1LL << 31) || (long long)M * N >= (1LL << 31))
+        return W4A16_ERR_SHAPE;
+    if (w == nullptr) return W4A16_ERR_NULL;
+    if (M > 0 && (x == nullptr || out == nullptr)) return W4A16_ERR_NULL;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(out)) return W4A16_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(bias) & 1u) != 0) return W4A16_ERR_ALIGN;
+    if (M == 0) return W4A16_OK;
+    const DeviceInfo *dev = nullptr;
+    int rc = get_device(&dev);
+    if (rc != W4A16_OK) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    bool pdl;
+    PrefillCfg c;
+    bool forced;
+    {
+        std::lock_guard<std::mutex> lk(g_cfg_mu);
+        pdl = g_pdl != 0;
+        forced = g_prefill_override;
+        c = g_prefill_cfg;
+    }
+    if (take_weights_written(s)) pdl = false;
+    if (!forced) c = prefill_dense_pick_cfg(M, N, K, *dev);
+    c.wstages = 0;
+    if (!prefill_dense_cfg_valid(c)) return W4A16_ERR_ARG;
+    GemmArgs a{x, nullptr, nullptr, nullptr, out, M, N, K, 0, dtype};
+    a.bias = bias;
+    a.wdense = w;
+    const cudaError_t e = launch_prefill(a, c, *dev, s, pdl);
+    char line[256];
+    std::snprintf(line, sizeof line,
+                  "gemm_dense M=%d N=%d K=%d %s path=prefill kernel=prefill_kernel(dense) BN=%d stages=%d ks=%d "
+                  "pdl=%d bias=%d%s",
+                  M, N, K, dtype == 0 ? "fp16" : "bf16", c.BN, c.stages, c.ks, pdl ? 1 : 0, bias != nullptr ? 1 : 0,
+                  forced ? " (forced)" : "");
+    log_selection(line);
+    return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
+}
+}  // namespace
+
+int w4a16_gemm_dense(const void *x, int M, int K, const void *w, int N, const void *bias_or_null, void *out,
+                     w4a16_dtype_t dtype, w4a16_stream_t stream) {
+    return run_gemm_dense(x, M, K, w, N, bias_or_null, out, (int)dtype, stream);
+}
+
+int w4a16_gemm_cached(const void *x, int M, int K, const int32_t *qweight, const void *scales,
+                      const int32_t *qzeros_or_null, int G, int N, const void *w_cache_or_null, void *out,
+                      w4a16_stream_t stream, w4a16_dtype_t dtype) {
+    int rc = validate_gemm(x, M, K, qweight, scales, qzeros_or_null, G, N, out, (int)dtype);
+    if (rc != W4A16_OK) return rc;
+    if (w_cache_or_null != nullptr &&
+        select_path_impl(M, N, K, G, qzeros_or_null == nullptr, (int)dtype) == W4A16_PATH_PREFILL)
+        return run_gemm_dense(x, M, K, w_cache_or_null, N, nullptr, out, (int)dtype, stream);
+    return run_gemm(x, M, K, qweight, scales, qzeros_or_null, G, N, out, stream, (int)dtype, W4A16_PATH_AUTO);
+}
+
 int w4a16_gemm_chain(const void *x, int M, const w4a16_layer_t *layers, int n_layers, w4a16_dtype_t dtype,
                      w4a16_stream_t stream) {
     if (n_layers < 0) return W4A16_ERR_ARG;

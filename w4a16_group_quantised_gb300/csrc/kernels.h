@@ -15,6 +15,7 @@ struct GemmArgs {
     int M, N, K, G;
     int dtype;              // 0 fp16, 1 bf16
     const void *bias = nullptr;  // [N] in the activation dtype, or none
+    const void *wdense = nullptr;  // prefill only: dtype W [N, K] (dequantised cache) instead of qweight
     int silu_mul = 0;       // 1: out [M, N/2] = silu(y[:, :N/2]) * y[:, N/2:] (rows 0..N/2-1 = gate)
 };
 
@@ -80,6 +81,10 @@ struct PrefillCfg {
     int ks = 0;   // CTAs of a cluster splitting K: 0 = chosen at launch, else 1..8
 };
 bool prefill_cfg_valid(const PrefillCfg &c);
+// dense form (wdense): no packed-weight ring (wstages unused)
+bool prefill_dense_cfg_valid(const PrefillCfg &c);
+PrefillCfg prefill_dense_pick_cfg(int M, int N, int K, const DeviceInfo &dev);
+int prefill_dense_best_ks(const PrefillCfg &base, long long tiles, int K, const DeviceInfo &dev, double *cost);
 PrefillCfg prefill_pick_cfg(int M, int N, int K, int G, int sym, int dtype, const DeviceInfo &dev);
 cudaError_t launch_prefill(const GemmArgs &a, const PrefillCfg &c, const DeviceInfo &dev,
                            cudaStream_t s, bool pdl);

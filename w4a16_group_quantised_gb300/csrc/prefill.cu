@@ -41,6 +41,11 @@
 //    (r + 1) BN / KS) of the tile (deterministic; KS = 1 is the plain path).
 //    The host picks BN and KS with a time model fitted to this kernel and
 //    the GPU's cluster occupancy.
+//  * Dense form (the dequantised prefill cache): the weight operand is a
+//    dtype matrix W [N, K] already holding RN((q - z) s); warp 3 loads its
+//    64-k steps (two 128-row boxes, 128-byte swizzle: exactly the canonical
+//    layout the dequantisers would write) straight into the A ring, and
+//    warps 4..11 only run the epilogue.
 //  * Every mbarrier wait is bounded (%globaltimer); a wait that runs out sets
 //    the device status word and a CTA abort flag, and every role leaves its
 //    loop, so the CTA still frees its TMEM and exits.
@@ -119,7 +124,7 @@ __host__ __device__ inline bool prefill_epilogue_fits(int BN, int SX, int SA) {
     return (uint32_t)BN * kBW * 2 <= (uint32_t)SX * BN * 128 + (uint32_t)SA * kATileBytes;
 }
 
-template <int DT, bool ASYM>
+template <int DT, bool ASYM, bool DENSE>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_out, const PrefillParams p) {
@@ -165,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(xempty(s), 1);             // MMA commit
         }
         for (int a = 0; a < SA; ++a) {
-            mbar_init(afull(a), kDeqWarps);      // one arrive per dequant warp
+            mbar_init(afull(a), DENSE ? 1 : kDeqWarps);   // the TMA's arrive, or one per dequant warp
             mbar_init(aempty(a), 1);             // MMA commit
         }
         for (int w = 0; w < SW; ++w) {
@@ -202,6 +207,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait_bounded(xempty(s), (uint32_t)((i / SX) & 1) ^ 1u, p.status, abort_flag)) break;
                 mbar_arrive_expect_tx(xfull(s), xtx);
                 tma_load_2d(x_base + (uint32_t)s * p.BN * 128u, &tmap_x, xfull(s), (is0 + i) * kBK, m0);
+            }
+        }
+    } else if (warp == 3 && DENSE) {
+        // ------------------------------------------------------------ dense weight producer
+        // 64-k steps of the dtype weight cache straight into the A ring.
+        if (lane == 0) {
+            for (int i = 0; i < nk; ++i) {
+                const int a = i % SA;
+                if (!mbar_wait_bounded(aempty(a), (uint32_t)((i / SA) & 1) ^ 1u, p.status, abort_flag)) break;
+                mbar_arrive_expect_tx(afull(a), (uint32_t)kATileBytes);
+                const uint32_t dst = a_base + (uint32_t)a * kATileBytes;
+                tma_load_2d(dst, &tmap_w, afull(a), (is0 + i) * kBK, n0);
+                tma_load_2d(dst + kHalf * 128u, &tmap_w, afull(a), (is0 + i) * kBK, n0 + kHalf);
             }
         }
     } else if (warp == 3) {
@@ -241,6 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp >= 4) {
+        bool ok = true;
+        if constexpr (!DENSE) {
         // ------------------------------------------------------------ dequantisers
         const int r = threadIdx.x - 128;               // weight row within the tile, 0..255
         const int n = n0 + r;
@@ -327,7 +347,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                sw * 128u;
         const uint32_t w_row = (uint32_t)(r >> 3) * 1024u + sw * 128u;   // packed tile, same swizzle
         const DqConsts dc = p.dq;
-        bool ok = true;
         for (int i0 = 0; i0 < nk && ok; i0 += kStepsPerW) {
             unpack_tile_meta();
 #pragma unroll
@@ -384,6 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        }   // !DENSE
 
         // ------------------------------------------------------------ epilogue
         const bool have_acc = ok && mbar_wait_bounded(acc_bar, 0u, p.status, abort_flag);
@@ -573,6 +593,79 @@ PrefillCfg prefill_pick_cfg(int M, int N, int K, int G, int sym, int dtype, cons
     return best;
 }
 
+// ---- dense form (dequantised prefill cache): no packed-weight ring; the x
+// and A rings have the same depth.
+static bool prefill_dense_fits(const PrefillCfg &c) {
+    const SmemLayout L = prefill_layout(c.BN, c.stages, c.astages, 0);
+    return L.total <= 227 * 1024 && prefill_epilogue_fits(c.BN, c.stages, c.astages) &&
+           (c.ks <= 1 || (size_t)c.BN * kBW * 4 <= L.bar_off);
+}
+
+bool prefill_dense_cfg_valid(const PrefillCfg &c) {
+    if (c.BN < 16 || c.BN > 256 || c.BN % 16 != 0) return false;
+    if (c.stages < 2 || c.astages < 2) return false;
+    if (c.ks < 0 || c.ks > 8) return false;
+    return prefill_dense_fits(c);
+}
+
+// Time model of the dense form (microseconds): per 64-k step a CTA is bound
+// by the tensor cores (2 x 128 x BN x 64 MACs, about 0.55 BN / 256 us at
+// the measured bf16 rate) or by fetching its operands (32 KB of weights and
+// BN x 128 B of x, about 0.2 us per step from L2 / HBM), plus 4 us of
+// start-up and epilogue and the cluster reduction when K is split.
+static double prefill_dense_cost(int bn, int ks, long long tiles, int K, const DeviceInfo &dev) {
+    const int resident = dev.prefill_clusters[ks];
+    if (resident <= 0) return 1e30;
+    const long long waves = (tiles + resident - 1) / resident;
+    const int nwt = (K + kWK - 1) / kWK;
+    const int steps = ((nwt + ks - 1) / ks) * kStepsPerW;
+    const double step = std::max(0.55 * bn / 256.0, 0.2);
+    return (double)waves * (steps * step + 4.0 + (ks > 1 ? 1.0 + bn / 64.0 : 0.0));
+}
+
+int prefill_dense_best_ks(const PrefillCfg &base, long long tiles, int K, const DeviceInfo &dev, double *cost) {
+    const int nwt = (K + kWK - 1) / kWK;
+    int best = 1;
+    double best_cost = 1e30;
+    for (int ks = 1; ks <= 8 && ks <= nwt; ++ks) {
+        PrefillCfg c = base;
+        c.ks = ks;
+        if (!prefill_dense_fits(c)) continue;
+        const double t = prefill_dense_cost(c.BN, ks, tiles, K, dev);
+        if (t < best_cost * 0.995) {
+            best_cost = t;
+            best = ks;
+        }
+    }
+    if (cost) *cost = best_cost;
+    return best;
+}
+
+PrefillCfg prefill_dense_pick_cfg(int M, int N, int K, const DeviceInfo &dev) {
+    const int ntiles_n = (N + kBW - 1) / kBW;
+    const int bn_max = std::min(256, std::max(16, (M + 15) / 16 * 16));
+    PrefillCfg best{bn_max, 2, 2, 0, 1};
+    double best_cost = 1e30;
+    for (int bn = 16; bn <= bn_max; bn += 16) {
+        PrefillCfg c{bn, 2, 2, 0, 1};
+        for (int st = 4; st >= 2; --st) {        // the deepest rings that fit with room for a split
+            c.stages = c.astages = st;
+            c.ks = 2;
+            if (prefill_dense_fits(c)) break;
+        }
+        c.ks = 1;
+        if (!prefill_dense_fits(c)) continue;
+        const long long tiles = (long long)((M + bn - 1) / bn) * ntiles_n;
+        double t = 0.0;
+        c.ks = prefill_dense_best_ks(c, tiles, K, dev, &t);
+        if (t < best_cost * 0.995) {
+            best_cost = t;
+            best = c;
+        }
+    }
+    return best;
+}
+
 bool prefill_cfg_valid(const PrefillCfg &c) {
     if (c.BN < 16 || c.BN > 256 || c.BN % 16 != 0) return false;
     if (c.stages < 2 || c.astages < 2 || c.wstages < 2) return false;
@@ -581,10 +674,10 @@ bool prefill_cfg_valid(const PrefillCfg &c) {
     return prefill_cfg_fits(c);
 }
 
-template <int DT, bool ASYM>
+template <int DT, bool ASYM, bool DENSE>
 static cudaError_t launch_t(const CUtensorMap &tx, const CUtensorMap &tw, const CUtensorMap &to,
                             const PrefillParams &p, size_t smem, int grid, cudaStream_t s, bool pdl) {
-    auto kern = prefill_kernel<DT, ASYM>;
+    auto kern = prefill_kernel<DT, ASYM, DENSE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -616,8 +709,9 @@ static cudaError_t launch_t(const CUtensorMap &tx, const CUtensorMap &tw, const 
 // takes more than half an SM's shared memory, so one CTA per SM).
 cudaError_t prefill_prepare_device(DeviceInfo &dev) {
     const int smem = dev.max_smem_optin;
-    decltype(&prefill_kernel<0, false>) kerns[4] = {
-        prefill_kernel<0, false>, prefill_kernel<0, true>, prefill_kernel<1, false>, prefill_kernel<1, true>};
+    decltype(&prefill_kernel<0, false, false>) kerns[6] = {
+        prefill_kernel<0, false, false>, prefill_kernel<0, true, false>, prefill_kernel<1, false, false>,
+        prefill_kernel<1, true, false>, prefill_kernel<0, false, true>, prefill_kernel<1, false, true>};
     for (auto k : kerns) {
         const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
@@ -648,7 +742,8 @@ cudaError_t prefill_prepare_device(DeviceInfo &dev) {
 cudaError_t launch_prefill(const GemmArgs &a, const PrefillCfg &c, const DeviceInfo &dev,
                            cudaStream_t s, bool pdl) {
     if (dev.encode_tiled == nullptr) return cudaErrorNotSupported;
-    if (!prefill_cfg_valid(c)) return cudaErrorInvalidValue;
+    const bool dense = a.wdense != nullptr;
+    if (dense ? !prefill_dense_cfg_valid(c) : !prefill_cfg_valid(c)) return cudaErrorInvalidValue;
     EncodeTiledFn encode = reinterpret_cast<EncodeTiledFn>(dev.encode_tiled);
     const CUtensorMapDataType act = a.dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                  : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -663,7 +758,17 @@ cudaError_t launch_prefill(const GemmArgs &a, const PrefillCfg &c, const DeviceI
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    {
+    if (dense) {
+        // W [N, K] in the activation dtype: 64-k x 128-row boxes, 128-byte swizzle
+        cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.N};
+        cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
+        cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kHalf};
+        cuuint32_t estr[2] = {1, 1};
+        if (encode(&tw, act, 2, const_cast<void *>(a.wdense), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    } else {
         cuuint64_t dims[2] = {(cuuint64_t)(a.K / 8), (cuuint64_t)a.N};
         cuuint64_t strides[1] = {(cuuint64_t)(a.K / 8) * 4};
         cuuint32_t box[2] = {(cuuint32_t)(kWK / 8), (cuuint32_t)kBW};
@@ -692,33 +797,36 @@ cudaError_t launch_prefill(const GemmArgs &a, const PrefillCfg &c, const DeviceI
     p.M = a.M;
     p.N = a.N;
     p.K = a.K;
-    p.G = a.G;
-    p.ng = a.K / a.G;
+    p.G = dense ? 0 : a.G;
+    p.ng = dense ? 0 : a.K / a.G;
     p.BN = c.BN;
     p.SX = c.stages;
     p.SA = c.astages;
-    p.SW = c.wstages;
+    p.SW = dense ? 0 : c.wstages;
     p.n_mtiles = (a.M + c.BN - 1) / c.BN;
     p.status = dev.status;
     const int n_ntiles = (a.N + kBW - 1) / kBW;
-    const SmemLayout L = prefill_layout(c.BN, c.stages, c.astages, c.wstages);
+    const SmemLayout L = prefill_layout(c.BN, c.stages, c.astages, dense ? 0 : c.wstages);
     // Too few output tiles to fill the SMs (small M): split K over a cluster
     // of KS CTAs, each summing whole packed-weight tiles, as long as every
     // CTA keeps at least one tile and the fp32 partial tile fits over the rings.
     const int tiles = n_ntiles * p.n_mtiles;
     const int nwt = (a.K + kWK - 1) / kWK;
     int ks = c.ks;
-    if (ks == 0) ks = prefill_best_ks(c, tiles, nwt, dev, nullptr);
+    if (ks == 0) ks = dense ? prefill_dense_best_ks(c, tiles, a.K, dev, nullptr) : prefill_best_ks(c, tiles, nwt, dev, nullptr);
     ks = std::max(1, std::min(ks, nwt));
     p.KS = ks;
     const int grid = tiles * ks;
     const size_t smem = L.total;
     const bool asym = a.qzeros != nullptr;
+    if (dense)
+        return a.dtype == 0 ? launch_t<0, false, true>(tx, tw, to, p, smem, grid, s, pdl)
+                            : launch_t<1, false, true>(tx, tw, to, p, smem, grid, s, pdl);
     if (a.dtype == 0)
-        return asym ? launch_t<0, true>(tx, tw, to, p, smem, grid, s, pdl)
-                    : launch_t<0, false>(tx, tw, to, p, smem, grid, s, pdl);
-    return asym ? launch_t<1, true>(tx, tw, to, p, smem, grid, s, pdl)
-                : launch_t<1, false>(tx, tw, to, p, smem, grid, s, pdl);
+        return asym ? launch_t<0, true, false>(tx, tw, to, p, smem, grid, s, pdl)
+                    : launch_t<0, false, false>(tx, tw, to, p, smem, grid, s, pdl);
+    return asym ? launch_t<1, true, false>(tx, tw, to, p, smem, grid, s, pdl)
+                : launch_t<1, false, false>(tx, tw, to, p, smem, grid, s, pdl);
 }
 
 }  // namespace w4a16
