@@ -191,6 +191,34 @@ int w4a16_gemm_fused(const void *x, int M, int K, const int32_t *qweight, const 
                      int epilogue, void *out, w4a16_stream_t stream, w4a16_dtype_t dtype,
                      w4a16_path_t path);
 
+/* MoE grouped skinny GEMM: the decode kernel over routed experts.
+ * Source: "Upstream sync 67/N: merge 382bbd5144 HybridW4A16LinearKernel
+ * (conflict)", the conflict table's csrc/rocm/ops.h row and the closing
+ * section (fused_moe_wvSplitK_int4_gemm: the MoE version of the skinny
+ * GEMM).  The pages give only its name; its result here is
+ *   out[t, j, :] = x[t, :] . dequant(W_e)^T  (* route_weights[t, j]),
+ *   e = expert_ids[t, j], 0 <= t < T, 0 <= j < topk,
+ * with each expert's weight as in w4a16_gemm (RN((q - z) s) weights, fp32
+ * accumulation, one rounding of the result).
+ *  x            device [T, K] activations (`dtype`);
+ *  qweight      device [E, N, K/8] int32, the experts' packed weights stacked;
+ *  scales       device [E, N, K/G] (`dtype`);
+ *  qzeros_or_null  device [E, N/8, K/G] int32, or NULL (symmetric);
+ *  expert_ids   device [T, topk] int32 (read by the kernel: it may be the
+ *               output of the kernel before it on the stream); an id outside
+ *               [0, E) gives a zero output row and W4A16_ERR_ARG in the
+ *               device status word (w4a16_last_device_error);
+ *  route_weights_or_null  device [T, topk] fp32 factors, or NULL;
+ *  out          device [T, topk, N] (`dtype`).
+ * Requirements as w4a16_gemm for N, K, G and the 16-byte alignment of x,
+ * qweight, scales, qzeros and out (expert_ids and route weights: 4 bytes);
+ * T >= 0 (T == 0 is a no-op), topk >= 1, E >= 1; W4A16_ERR_SHAPE beyond
+ * int32 index range. */
+int w4a16_moe_gemm(const void *x, int T, int K, const int32_t *qweight, const void *scales,
+                   const int32_t *qzeros_or_null, int G, int N, int E, const int32_t *expert_ids,
+                   int topk, const float *route_weights_or_null, void *out, w4a16_dtype_t dtype,
+                   w4a16_stream_t stream);
+
 /* Dequantised prefill cache.  Source: "[ROCm] Converge the two W4A16 linear
  * kernels onto the upstream shell", section "What this does": an optional
  * dequantised copy of the weight that prefill reads with a plain dtype GEMM,

@@ -186,6 +186,29 @@ def epilogue(y, N: int, dtype: int, bias=None, silu_mul: bool = False) -> np.nda
     return out
 
 
+def moe_gemm(x, T: int, K: int, qweight, scales, qzeros, G: int, N: int, expert_ids, dtype: int,
+             route_weights=None) -> np.ndarray:
+    """Grouped skinny GEMM over routed experts, float64 [T, topk, N]:
+    out[t, j] = x[t] . W_ref(e)^T with e = expert_ids[t, j], the expert's
+    weight W_ref(e) = RN_dtype((q - z) * s) from qweight[e] [N, K/8],
+    scales[e] [N, K/G] and qzeros[e] [N/8, K/G] (or symmetric), times
+    route_weights[t, j] when given.  Each (token, expert) pair is one call of
+    gemm() above on that token's row and that expert's slices."""
+    x = _c(x, np.uint16).reshape(T, K)
+    ids = np.asarray(expert_ids, dtype=np.int64).reshape(T, -1)
+    topk = ids.shape[1]
+    out = np.zeros((T, topk, N), dtype=np.float64)
+    for t in range(T):
+        for j in range(topk):
+            e = int(ids[t, j])
+            y = gemm(x[t:t + 1], 1, K, qweight[e], scales[e], None if qzeros is None else qzeros[e], G, N,
+                     dtype)[0]
+            if route_weights is not None:
+                y = y * float(np.asarray(route_weights, dtype=np.float64).reshape(T, topk)[t, j])
+            out[t, j] = y
+    return out
+
+
 def num_threads() -> int:
     return _load().oracle_num_threads()
 

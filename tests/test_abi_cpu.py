@@ -266,3 +266,20 @@ def test_cache_entry_point_limits(lib):
         [ctypes.c_void_p] * 3 + [ctypes.c_int]
     assert h(ALIGNED, 1, 128, ALIGNED, ALIGNED, None, 48, 64, ALIGNED, ALIGNED, None, 0) == -3
     assert h(None, 0, 128, ALIGNED, ALIGNED, None, 32, 64, ALIGNED, None, None, 0) == 0
+
+
+def test_moe_entry_point_limits(lib):
+    f = lib.w4a16_moe_gemm
+    P, I = ctypes.c_void_p, ctypes.c_int
+    f.argtypes = [P, I, I, P, P, P, I, I, I, P, I, P, P, I, P]
+    call = lambda T=1, K=128, G=32, N=64, E=4, ids=ALIGNED, topk=2, rw=None, x=ALIGNED: f(
+        x, T, K, ALIGNED, ALIGNED, None, G, N, E, ids, topk, rw, ALIGNED, 0, None)
+    assert call(E=0) == -2
+    assert call(topk=0) == -2
+    assert call(T=-1) == -2
+    assert call(N=60) == -2
+    assert call(G=48) == -3
+    assert call(ids=None) == -1
+    assert call(rw=ctypes.c_void_p(0x1002)) == -4
+    assert call(x=MISALIGNED) == -4
+    assert call(T=0, ids=None, x=None) == 0

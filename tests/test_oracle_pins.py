@@ -323,3 +323,48 @@ def test_epilogue_silu_mul_against_torch():
     # the halves are not interchangeable: swapping them changes the result
     swapped = torch.nn.functional.silu(a[:, 32:]) * a[:, :32]
     assert not np.allclose(h, swapped.numpy())
+
+
+# --------------------------------------------------------------------- MoE
+def _experts(E, N, K, G, sym, dtype, seed):
+    ps = [make_problem(1, N, K, G, sym, dtype, seed=seed + e) for e in range(E)]
+    qw = np.stack([oracle.pack(p.q) for p in ps])
+    sc = np.stack([p.scales for p in ps])
+    qz = None if sym else np.stack([oracle.pack_zeros(p.z) for p in ps])
+    return ps, qw, sc, qz
+
+
+def test_moe_single_expert_is_the_gemm():
+    """One expert, every token routed to it: the MoE result is the plain
+    GEMM of all tokens (the pinned routine), row for row."""
+    ps, qw, sc, qz = _experts(1, 16, 64, 32, False, F16, 51)
+    x = make_problem(3, 16, 64, 32, False, F16, seed=52).x
+    got = oracle.moe_gemm(x, 3, 64, qw, sc, qz, 32, 16, np.zeros((3, 2), np.int32), F16)
+    want = oracle.gemm(x, 3, 64, qw[0], sc[0], qz[0], 32, 16, F16)
+    assert np.array_equal(got[:, 0], want) and np.array_equal(got[:, 1], want)
+
+
+def test_moe_brute_force_and_routing():
+    """Against a numpy restatement (unpack, RN of (q - z) s through torch,
+    float64 dot products) on routed tokens with repeated experts and routing
+    weights; relabelling the experts (permuting the weight stack and the ids
+    alike) changes nothing."""
+    E, N, K, G = 4, 8, 64, 32
+    ps, qw, sc, qz = _experts(E, N, K, G, False, BF16, 61)
+    x = make_problem(3, N, K, G, False, BF16, seed=62).x
+    ids = np.array([[2, 0], [1, 1], [3, 2]], dtype=np.int32)
+    rw = np.array([[0.25, 0.75], [1.0, -0.5], [2.0, 0.125]])
+    got = oracle.moe_gemm(x, 3, K, qw, sc, qz, G, N, ids, BF16, route_weights=rw)
+    xv = (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    for t in range(3):
+        for j in range(2):
+            p = ps[ids[t, j]]
+            q = p.q.astype(np.int64)
+            z = np.repeat(p.z.astype(np.int64), G, axis=1)
+            s = (np.repeat(p.scales, G, axis=1).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+            wv = torch.from_numpy((q - z) * s).to(torch.bfloat16).to(torch.float64).numpy()
+            np.testing.assert_allclose(got[t, j], (wv @ xv[t]) * rw[t, j], rtol=1e-12, atol=1e-12)
+    perm = np.array([3, 1, 0, 2])                 # new expert i is old expert perm[i]
+    inv = np.argsort(perm)
+    got2 = oracle.moe_gemm(x, 3, K, qw[perm], sc[perm], qz[perm], G, N, inv[ids], BF16, route_weights=rw)
+    assert np.array_equal(got, got2)

@@ -61,6 +61,7 @@ def load_library():
             "w4a16_gemm_fused": [P, I, I, P, P, P, I, I, P, I, P, P, I, I],
             "w4a16_gemm_chain": [P, I, P, I, I, P],
             "w4a16_dequantize": [P, P, P, I, I, I, P, I, P],
+            "w4a16_moe_gemm": [P, I, I, P, P, P, I, I, I, P, I, P, P, I, P],
             "w4a16_gemm_dense": [P, I, I, P, I, P, P, I, P],
             "w4a16_gemm_cached": [P, I, I, P, P, P, I, I, P, P, P, I],
             "w4a16_gemm_host": [P, I, I, P, P, P, I, I, P, I, P, P, P],
@@ -246,6 +247,44 @@ def w4a16_gemm_fused(x, qweight, scales, qzeros, G: int, bias=None, epilogue: in
     rc = lib.w4a16_gemm_fused(_p(x), M, K, _p(qweight), _p(scales), _p(qzeros), G, N, _p(bias), epilogue,
                               _p(out), _stream_ptr(stream), dt, path)
     _check("w4a16_gemm_fused", rc)
+    return out
+
+
+def w4a16_moe_gemm(x, qweight, scales, qzeros, G: int, expert_ids, route_weights=None, out=None, stream=None):
+    """MoE grouped skinny GEMM: out [T, topk, N] with out[t, j] = x[t] .
+    dequant(W_{expert_ids[t, j]})^T (* route_weights[t, j]); qweight
+    [E, N, K/8], scales [E, N, K/G], qzeros [E, N/8, K/G] or None."""
+    import torch
+    for name, t in (("x", x), ("qweight", qweight), ("scales", scales), ("qzeros", qzeros),
+                    ("expert_ids", expert_ids), ("route_weights", route_weights), ("out", out)):
+        if t is not None and (not isinstance(t, torch.Tensor) or t.device.type != "cuda" or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    _require_int32("qweight", qweight)
+    _require_int32("qzeros", qzeros)
+    dt = _dtype_code(x)
+    if scales.dtype != x.dtype:
+        raise TypeError("scales must have the dtype of x")
+    if expert_ids.dtype != torch.int32 or expert_ids.dim() != 2:
+        raise TypeError("expert_ids must be int32 [T, topk]")
+    if route_weights is not None and (route_weights.dtype != torch.float32
+                                      or route_weights.shape != expert_ids.shape):
+        raise TypeError("route_weights must be float32 [T, topk]")
+    T, K = x.shape
+    E, N, K8 = qweight.shape
+    topk = expert_ids.shape[1]
+    if K8 * 8 != K or expert_ids.shape[0] != T:
+        raise ValueError("qweight must be [E, N, K/8] and expert_ids [T, topk]")
+    if G > 0 and K % G == 0 and list(scales.shape) != [E, N, K // G]:
+        raise ValueError(f"scales must be [E, N, K/G] = [{E}, {N}, {K // G}]")
+    if qzeros is not None and G > 0 and K % G == 0 and list(qzeros.shape) != [E, N // 8, K // G]:
+        raise ValueError(f"qzeros must be [E, N/8, K/G] = [{E}, {N // 8}, {K // G}]")
+    if out is None:
+        out = torch.empty((T, topk, N), dtype=x.dtype, device=x.device)
+    elif list(out.shape) != [T, topk, N] or out.dtype != x.dtype:
+        raise ValueError(f"out must be [{T}, {topk}, {N}] of x's dtype")
+    rc = load_library().w4a16_moe_gemm(_p(x), T, K, _p(qweight), _p(scales), _p(qzeros), G, N, E, _p(expert_ids),
+                                       topk, _p(route_weights), _p(out), dt, _stream_ptr(stream))
+    _check("w4a16_moe_gemm", rc)
     return out
 
 

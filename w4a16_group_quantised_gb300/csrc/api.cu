@@ -462,6 +462,58 @@ int w4a16_gemm_fused(const void *x, int M, int K, const int32_t *qweight, const 
                     bias_or_null, epilogue);
 }
 
+int w4a16_moe_gemm(const void *x, int T, int K, const int32_t *qweight, const void *scales,
+                   const int32_t *qzeros_or_null, int G, int N, int E, const int32_t *expert_ids, int topk,
+                   const float *route_weights_or_null, void *out, w4a16_dtype_t dtype, w4a16_stream_t stream) {
+    if (T < 0 || E < 1 || topk < 1) return W4A16_ERR_SHAPE;
+    int rc = validate_common(1, N, K, G, (int)dtype);
+    if (rc != W4A16_OK) return rc;
+    const long long slots = (long long)T * topk;
+    if ((long long)E * N * (K / 8) >= (1LL << 31) || (long long)E * N >= (1LL << 31) ||
+        slots * N >= (1LL << 31) || (long long)T * K >= (1LL << 31) || slots > (1LL << 24))
+        return W4A16_ERR_SHAPE;
+    if (qweight == nullptr || scales == nullptr) return W4A16_ERR_NULL;
+    if (T > 0 && (x == nullptr || out == nullptr || expert_ids == nullptr)) return W4A16_ERR_NULL;
+    if (!aligned16(qweight) || !aligned16(scales) || !aligned16(qzeros_or_null) || !aligned16(x) ||
+        !aligned16(out) || (reinterpret_cast<uintptr_t>(expert_ids) & 3u) != 0 ||
+        (reinterpret_cast<uintptr_t>(route_weights_or_null) & 3u) != 0)
+        return W4A16_ERR_ALIGN;
+    if (T == 0) return W4A16_OK;
+    const DeviceInfo *dev = nullptr;
+    rc = get_device(&dev);
+    if (rc != W4A16_OK) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    bool pdl, forced;
+    DecodeCfg c;
+    {
+        std::lock_guard<std::mutex> lk(g_cfg_mu);
+        pdl = g_pdl != 0;
+        forced = g_decode_override;
+        c = g_decode_cfg;
+    }
+    if (take_weights_written(s)) pdl = false;
+    const bool asym = qzeros_or_null != nullptr;
+    // the configuration of one layer with the rows of every routed slot
+    const int n_all = (int)std::min<long long>(slots * N, 1LL << 30);
+    if (!forced) c = decode_pick_cfg(1, n_all, K, G, !asym, (int)dtype, dev->sm_count, dev->smem_per_sm);
+    if (!decode_cfg_valid(c, 1, K, G, asym)) return W4A16_ERR_ARG;
+    GemmArgs a{x, qweight, scales, qzeros_or_null, out, 1, N, K, G, (int)dtype};
+    a.expert_ids = expert_ids;
+    a.route_w = route_weights_or_null;
+    a.n_experts = E;
+    a.topk = topk;
+    a.n_slots = (int)slots;
+    const cudaError_t e = launch_decode(a, c, *dev, s, pdl);
+    char line[320];
+    std::snprintf(line, sizeof line,
+                  "moe_gemm T=%d topk=%d E=%d N=%d K=%d G=%d %s %s path=decode kernel=decode_kernel(experts) R=%d "
+                  "NW=%d NB=%d NS=%d S=%d pdl=%d%s",
+                  T, topk, E, N, K, G, dtype == 0 ? "fp16" : "bf16", asym ? "asym" : "sym", c.R, c.NW, c.NB, c.NS,
+                  c.S, pdl ? 1 : 0, forced ? " (forced)" : "");
+    log_selection(line);
+    return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
+}
+
 int w4a16_dequantize(const int32_t *qweight, const void *scales, const int32_t *qzeros_or_null, int G, int N,
                      int K, void *w_out, w4a16_dtype_t dtype, w4a16_stream_t stream) {
     return w4a16_dequant_debug_ex(qweight, scales, qzeros_or_null, G, N, K, w_out, dtype, stream, W4A16_DQ_PREFILL);

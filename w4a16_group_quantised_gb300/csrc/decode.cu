@@ -40,6 +40,14 @@
 //    N = 2 I rows, the gate rows first) a CTA's RT rows are RT / 2 gate rows
 //    j0.. and the RT / 2 up rows I + j0.. (one TMA box over a [2][I] view of
 //    the rows), and it writes silu(gate) * up for its RT / 2 outputs.
+//  * Expert mode (the MoE grouped skinny GEMM): the weight is a stack of E
+//    experts, [E * N] rows, and the grid runs over (token, expert slot) x
+//    row tile x cluster rank; a CTA reads its slot's expert id (after the
+//    grid-dependency wait: the routing may come from the previous kernel),
+//    offsets its rows by e * N, multiplies that one token, and writes row
+//    `slot` of the [T * topk, N] output, scaled by the slot's routing weight
+//    when one is given.  An out-of-range id writes zeros and records
+//    W4A16_ERR_ARG in the status word.
 //  * Every mbarrier wait is bounded; on a timeout the status word is set and
 //    the CTA leaves its loop.
 #include <algorithm>
@@ -75,6 +83,10 @@ struct DecodeParams {
     int gmax;        // max groups per CTA slice
     int silu;        // SiLU-and-multiply epilogue: rows are [gate | up], I = N / 2 each
     int hold;        // test hook: issue no weight copies, so the bounded waits run out
+    // expert mode (expert_ids != null): x [T, K], out [T * topk, N], weights [E * N] rows
+    const int *expert_ids;   // [T * topk]
+    const float *route_w;    // [T * topk] or null
+    int n_experts, topk, tiles;
 };
 
 // Weight tensor maps: `one` loads one 128-k block of RT rows (2-D, exact
@@ -129,12 +141,31 @@ __global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ 
     const int NW = p.NW, NS = p.NS, S = p.S;
     const int RT = 16 * R * NW;
     const int rank = (S > 1) ? (int)cg::this_cluster().block_rank() : 0;
-    const int tile = blockIdx.x / S;
+    int tile = blockIdx.x / S;
     const int silu = p.silu;
     const int RH = RT / 2;                           // SiLU: gate (and up) rows per CTA
     const int I = p.N / 2;
-    const int n_tile0 = silu ? tile * RH : tile * RT;
     const int M = p.M, K = p.K, gmax = p.gmax, log2G = p.log2G;
+    // expert mode: this CTA's slot, its expert's first row, its token's x row and output row
+    const uint16_t *xg = p.x;
+    uint16_t *outg = p.out;
+    int row_base = 0, slot = 0;
+    bool bad_expert = false;
+    if (p.expert_ids != nullptr) {
+        slot = tile / p.tiles;
+        tile -= slot * p.tiles;
+        grid_dependency_wait();                      // the routing may be the previous kernel's output
+        int e = p.expert_ids[slot];
+        if (e < 0 || e >= p.n_experts) {
+            bad_expert = true;
+            e = 0;
+            if (threadIdx.x == 0 && rank == 0) atomicExch(p.status, kStatusBadArg);
+        }
+        row_base = e * p.N;
+        xg = p.x + (size_t)(slot / p.topk) * K;
+        outg = p.out + (size_t)slot * p.N;
+    }
+    const int n_tile0 = silu ? tile * RH : tile * RT;
     const DecodeSmem L = decode_layout(R, NW, NB, NS, M, p.xpitch, gmax, ASYM, S);
 
     grid_dependents_launch();
@@ -142,11 +173,11 @@ __global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ 
     // ---- K slice of this CTA, in 128-wide blocks
     const int b0 = (int)((long long)rank * p.nblk / S);
     const int b1 = (int)((long long)(rank + 1) * p.nblk / S);
-    const int nb = b1 - b0;
+    const int nb = bad_expert ? 0 : b1 - b0;
     const int nsteps = (nb + NB - 1) / NB;          // ring stages to consume
     const int g0 = (b0 * kBoxK) >> log2G;           // first group of the slice
     const int g1 = min(p.ng, (b1 * kBoxK + p.G - 1) >> log2G);
-    const int ngs = g1 - g0;
+    const int ngs = bad_expert ? 0 : g1 - g0;
 
     const uint32_t sbase = smem_u32(smem);
     const uint32_t ring = sbase + L.ring;
@@ -165,14 +196,14 @@ __global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ 
             if (silu)
                 tma_load_4d(sdst, &maps.wide, sfull, 0, n_tile0, 0, bb);
             else
-                tma_load_3d(sdst, &maps.wide, sfull, 0, n_tile0, bb);
+                tma_load_3d(sdst, &maps.wide, sfull, 0, row_base + n_tile0, bb);
         } else {
             for (int j = 0; j < nbox; ++j) {
                 const uint32_t d = sdst + (uint32_t)j * RT * kBoxRowBytes;
                 if (silu)
                     tma_load_3d(d, &maps.one, sfull, (bb + j) * (kBoxK / 8), n_tile0, 0);
                 else
-                    tma_load_2d(d, &maps.one, sfull, (bb + j) * (kBoxK / 8), n_tile0);
+                    tma_load_2d(d, &maps.one, sfull, (bb + j) * (kBoxK / 8), row_base + n_tile0);
             }
         }
     };
@@ -222,8 +253,9 @@ __global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ 
             // weight row of tile row r (SiLU: gate rows j0.., then up rows I + j0..)
             const int n = silu ? (r < RH ? n_tile0 + r : I + n_tile0 + (r - RH)) : n_tile0 + r;
             const bool vr = silu ? (n_tile0 + (r < RH ? r : r - RH) < I) : n < p.N;
-            const uint16_t *srow = p.scales + (size_t)(vr ? n : 0) * p.ng + g0;
-            const int32_t *zrow = ASYM ? p.qz + (size_t)((vr ? n : 0) >> 3) * p.ng + g0 : nullptr;
+            const int nr = row_base + (vr ? n : 0);     // row in the (expert-stacked) weight
+            const uint16_t *srow = p.scales + (size_t)nr * p.ng + g0;
+            const int32_t *zrow = ASYM ? p.qz + (size_t)(nr >> 3) * p.ng + g0 : nullptr;
             const int zsh = 4 * (n & 7);
             unsigned char *mw = smem + L.meta + (size_t)r * gmax * kES;
             for (int gg0 = gs; gg0 < ngs; gg0 += 4 * tpr) {
@@ -262,7 +294,7 @@ __global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ 
                 const int m = i / nch, c = i - (i / nch) * nch;
                 const int k = kbase + 8 * c;
                 uint4 v = make_uint4(0, 0, 0, 0);
-                if (k < K) v = *reinterpret_cast<const uint4 *>(p.x + (size_t)m * K + k);
+                if (k < K) v = *reinterpret_cast<const uint4 *>(xg + (size_t)m * K + k);
                 const int b = c >> 4, cc = c & 15;
                 const int pos = b * 16 + (cc & 3) * 4 + (cc >> 2);   // chunk 4t+w stored at 4w+t
                 uint4 o;
@@ -396,10 +428,11 @@ __global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ 
         __syncthreads();
         if (S > 1) mbar_wait_cluster_bounded(gbar, 0u, p.status, abort_flag);
         if (!silu) {
+            const float rw = p.route_w != nullptr ? p.route_w[slot] : 1.0f;
             for (int i = threadIdx.x; i < RT * M; i += blockDim.x) {
                 const int m = i / RT, row = i - (i / RT) * RT;
                 const int n = n_tile0 + row;
-                if (n < p.N) p.out[(size_t)m * p.N + n] = f32_to_dt<DT>(row_sum(m, row, n));
+                if (n < p.N) outg[(size_t)m * p.N + n] = f32_to_dt<DT>(row_sum(m, row, n) * rw);
             }
         } else {
             for (int i = threadIdx.x; i < RH * M; i += blockDim.x) {
@@ -624,7 +657,8 @@ cudaError_t launch_decode(const GemmArgs &a, const DecodeCfg &c, const DeviceInf
         EncodeTiledFn encode = reinterpret_cast<EncodeTiledFn>(dev.encode_tiled);
         // rows as [N] or, with SiLU, as [2][I] (a dimension of 2 with stride I rows)
         const int silu = a.silu_mul ? 1 : 0;
-        const cuuint64_t rows = silu ? (cuuint64_t)(a.N / 2) : (cuuint64_t)a.N;
+        const cuuint64_t rows = silu ? (cuuint64_t)(a.N / 2)
+                                     : (cuuint64_t)a.N * (a.expert_ids != nullptr ? (cuuint64_t)a.n_experts : 1);
         const cuuint64_t row_bytes = (cuuint64_t)(a.K / 8) * 4;
         const cuuint32_t box_rows = silu ? (cuuint32_t)(RT / 2) : (cuuint32_t)RT;
         cuuint64_t dims[3] = {(cuuint64_t)(a.K / 8), rows, 2};
@@ -659,6 +693,10 @@ cudaError_t launch_decode(const GemmArgs &a, const DecodeCfg &c, const DeviceInf
     p.bias = (const uint16_t *)a.bias;
     p.silu = a.silu_mul ? 1 : 0;
     p.hold = hold_copies ? 1 : 0;
+    p.expert_ids = a.expert_ids;
+    p.route_w = a.route_w;
+    p.n_experts = a.n_experts;
+    p.topk = a.topk;
     p.status = dev.status;
     p.dq = dq_consts_i4(a.dtype);
     p.M = a.M;
@@ -676,7 +714,10 @@ cudaError_t launch_decode(const GemmArgs &a, const DecodeCfg &c, const DeviceInf
     p.xpitch = decode_xpitch(c, a.K);
     p.gmax = decode_gmax(c, a.K, a.G);
     const int tiles = a.silu_mul ? (a.N / 2 + RT / 2 - 1) / (RT / 2) : (a.N + RT - 1) / RT;
-    const int grid = tiles * c.S;
+    p.tiles = tiles;
+    const long long grid_ll = (long long)tiles * c.S * (a.expert_ids != nullptr ? a.n_slots : 1);
+    if (grid_ll > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
+    const int grid = (int)grid_ll;
     const size_t smem = decode_smem_bytes(c, a.M, a.K, a.G, asym);
     return launch_dispatch(a.dtype, asym, c.R, c.NB, tw, p, c, smem, s, pdl, grid);
 }

@@ -16,6 +16,11 @@ struct GemmArgs {
     int dtype;              // 0 fp16, 1 bf16
     const void *bias = nullptr;  // [N] in the activation dtype, or none
     const void *wdense = nullptr;  // prefill only: dtype W [N, K] (dequantised cache) instead of qweight
+    // decode expert mode (MoE): qweight/scales/qzeros stack n_experts experts of N rows;
+    // x [T, K], out [n_slots = T * topk, N], expert_ids / route_w [n_slots] on the device
+    const int *expert_ids = nullptr;
+    const float *route_w = nullptr;
+    int n_experts = 0, topk = 0, n_slots = 0;
     int silu_mul = 0;       // 1: out [M, N/2] = silu(y[:, :N/2]) * y[:, N/2:] (rows 0..N/2-1 = gate)
 };
 

@@ -7,6 +7,7 @@ namespace w4a16 {
 
 // Status word values written by kernels (same numbers as w4a16_status_t).
 constexpr int kStatusTimeout = -8;
+constexpr int kStatusBadArg = -9;      // W4A16_ERR_ARG: an argument only the device sees (an expert id)
 
 // A bounded wait gives up after this many nanoseconds of %globaltimer.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
