@@ -413,6 +413,67 @@ def bench_prefill_cache(w, M, steps, reps=5):
                 per_shape_us={n: round(t * 1e6, 2) for (n, _, _), t in zip(shapes, per_s)})
 
 
+def bench_moe(w, hbm, T=1, topk=8, E=128, steps_per_graph=48, reps=20):
+    """MoE decode on Qwen3-30B-A3B-like experts (128 experts, top-8, bf16,
+    symmetric, G = 128): per step one grouped GEMM over the experts' gate_up
+    (1536 x 2048) and one over their down (2048 x 768), each step with its own
+    seeded routing (a different id buffer per step in the graph), so the
+    experts' weights (about 300 MB in all) stream from HBM.  Algorithmic
+    bytes per step: the routed experts' packed weights and scales (each
+    (token, expert) pair counted: a repeated pair is re-read), x and y."""
+    shapes = [("experts gate_up", 1536, 2048), ("experts down", 2048, 768)]
+    G = 128
+    stacks = []
+    for si, (name, N, K) in enumerate(shapes):
+        q = torch.randint(0, 16, (E * N, K), dtype=torch.uint8,
+                          generator=torch.Generator(device="cuda").manual_seed(si), device="cuda")
+        qw = w.w4a16_pack(q).view(E, N, K // 8)
+        del q
+        sc = (torch.rand((E, N, K // G), generator=torch.Generator().manual_seed(10 + si)) * 0.018 + 0.002)
+        stacks.append(dict(N=N, K=K, qweight=qw, scales=sc.to(torch.bfloat16).cuda()))
+    rng = np.random.default_rng(7)
+    ids = [torch.from_numpy(np.stack([rng.choice(E, topk, replace=False) for _ in range(T)]).astype(np.int32)).cuda()
+           for _ in range(steps_per_graph)]
+    rw = torch.full((T, topk), 1.0 / topk, dtype=torch.float32, device="cuda")
+    x0 = torch.randn((T, shapes[0][2]), generator=torch.Generator().manual_seed(3)).to(torch.bfloat16).cuda()
+    x1 = torch.randn((T * topk, shapes[1][2]), generator=torch.Generator().manual_seed(4)).to(torch.bfloat16).cuda()
+    outs = [torch.empty((T, topk, N), dtype=torch.bfloat16, device="cuda") for (_, N, _) in shapes]
+
+    def step(i):
+        a, b = stacks
+        w.w4a16_moe_gemm(x0, a["qweight"], a["scales"], None, G, ids[i], out=outs[0])
+        # down: each (token, slot) row is its own token routed to its expert once
+        w.w4a16_moe_gemm(x1, b["qweight"], b["scales"], None, G, ids[i].view(T * topk, 1), route_weights=rw.view(-1, 1),
+                         out=outs[1].view(T * topk, 1, -1))
+
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        step(0)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(steps_per_graph):
+                step(i)
+        g.replay()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) / 1e3 / steps_per_graph)
+    dt = statistics.median(ts)
+    per_pair = sum(N * K // 2 + N * (K // G) * 2 for (_, N, K) in shapes)
+    step_bytes = T * topk * per_pair + T * shapes[0][2] * 2 + T * topk * (shapes[0][1] + shapes[1][2] + shapes[1][1]) * 2
+    del stacks, ids, outs
+    torch.cuda.empty_cache()
+    return {"workload": f"moe-decode T={T} top{topk} of {E} experts, gate_up 1536x2048 + down 2048x768, bf16 sym G128",
+            "step_us": round(dt * 1e6, 3), "GB/s": round(step_bytes / dt / 1e9, 1),
+            "frac": round(step_bytes / dt / 1e9 / hbm, 4), "step_bytes": step_bytes}
+
+
 def profile_case(w, which, steps, warmup, m=None):
     """A short run for ncu captures: `warmup` then `steps` eager passes over
     the four layers of one workload (one set of inputs, launched in layer
@@ -585,6 +646,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the extra workloads (Llama decode, M sweep, M=128 prefill)")
+    ap.add_argument("--no-median", action="store_true",
+                    help="skip the per-shape and whole-step median replays of the decode layers")
     ap.add_argument("--profile-case", choices=["decode", "prefill"],
                     help="run only the short eager case that ncu captures")
     ap.add_argument("--profile-m", type=int, default=None,
@@ -655,7 +718,7 @@ def main():
     launches = steps * len(qshapes)
     per_launch_s = dt / launches
     achieved = st.step_bytes / len(qshapes) / per_launch_s / 1e9
-    qsum = stream_summary(st, hbm, [n for (n, _, _) in qshapes])
+    qsum = None if args.no_median else stream_summary(st, hbm, [n for (n, _, _) in qshapes])
 
     e2e = None
     if not args.no_e2e:
@@ -687,6 +750,7 @@ def main():
             r["per_shape"][name]["TFLOP/s"] = round(2 * 128 * N * K / (r["per_shape"][name]["us"] * 1e-6) / 1e12, 1)
         r["TFLOP/s"] = round(sum(2 * 128 * N * K for (_, N, K) in lshapes) / (r["step_us"] * 1e-6) / 1e12, 1)
         extra["prefill_llama31_8b_m128"] = dict(workload="llama-3.1-8b-prefill-m128-asym-g64-bf16", **r)
+        extra["moe_decode"] = bench_moe(w, hbm)
         for Mc in (1920, 128):
             rc = bench_prefill_cache(w, Mc, max(2, args.prefill_steps))
             extra[f"prefill_dense_cache_m{Mc}"] = dict(
@@ -743,7 +807,7 @@ def main():
                      "kernel": "decode_kernel (split-K skinny GEMM; all four launches)",
                      "per_launch_us": round(per_launch_s * 1e6, 3),
                      "bytes_per_launch": st_bytes_mean(qshapes)},
-        "decode_median": qsum,
+        "decode_median": qsum,       # per-shape and whole-step medians (null with --no-median)
         "prefill": {"workload": PREFILL_WORKLOAD, "value": round(pre["tflops"], 2), "unit": "TFLOP/s",
                     "ms_per_step": round(pre["ms_per_step"], 4),
                     "per_shape_tflops": {n: round(v, 1) for (n, _, _), v in

@@ -349,6 +349,30 @@ int run_gemm(const void *x, int M, int K, const int32_t *qw, const void *scales,
 
 }  // namespace
 
+cudaError_t raise_smem_cap(const void *func, size_t need) {
+    struct Entry {
+        const void *func;
+        int device;
+    };
+    static std::mutex mu;
+    static Entry done[256];
+    static int n_done = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < n_done; ++i)
+        if (done[i].func == func && done[i].device == dev) return cudaSuccess;   // already at the maximum
+    int optin = 0;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    if (need > (size_t)optin) return cudaErrorInvalidValue;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    if (e != cudaSuccess) return e;
+    if (n_done < 256) done[n_done++] = Entry{func, dev};
+    return cudaSuccess;
+}
+
 // Shared with the allocation-free entry point (noalloc.cu): the same host
 // validation, and the status word's device address (no device state is
 // created here).

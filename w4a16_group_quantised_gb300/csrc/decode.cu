@@ -592,7 +592,7 @@ static cudaError_t launch_t(const DecodeMaps &tw, const DecodeParams &p, const D
                             size_t smem, cudaStream_t s, bool pdl, int grid) {
     auto kern = decode_kernel<DT, ASYM, R, NB>;
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = raise_smem_cap(reinterpret_cast<const void *>(kern), smem);
         if (e != cudaSuccess) return e;
     }
     cudaLaunchConfig_t cfg = {};

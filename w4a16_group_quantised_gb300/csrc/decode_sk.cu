@@ -366,7 +366,7 @@ static cudaError_t launch_sk_t(const int32_t *qw, const sk::Params &p, size_t sm
                                cudaStream_t s, bool pdl) {
     auto kern = sk::decode_sk_kernel<DT, ASYM, NS>;
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = raise_smem_cap(reinterpret_cast<const void *>(kern), smem);
         if (e != cudaSuccess) return e;
     }
     cudaLaunchConfig_t cfg = {};

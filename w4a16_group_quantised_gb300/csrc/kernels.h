@@ -68,6 +68,14 @@ bool decode_sk_applicable(int M, int K);
 cudaError_t launch_decode_sk(const GemmArgs &a, int ns, const DeviceInfo &dev, float *ws, int *counters,
                              cudaStream_t s, bool pdl);
 
+// Make sure kernel `func` may launch with `need` bytes of dynamic shared
+// memory on the current device.  The cap is a property of the function,
+// shared by every launch of it and read again whenever a captured graph node
+// of it is launched on its own (as a profiler does), so it is set once to
+// the device's opt-in maximum and never lowered: setting it per launch let a
+// smaller launch lower it under a graph node captured with a larger one.
+cudaError_t raise_smem_cap(const void *func, size_t need);
+
 // ---- api.cu helpers used by noalloc.cu
 int validate_gemm_args(const void *x, int M, int K, const int32_t *qw, const void *scales, const int32_t *qz,
                        int G, int N, const void *out, int dtype);

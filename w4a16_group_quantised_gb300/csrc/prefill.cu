@@ -678,7 +678,7 @@ template <int DT, bool ASYM, bool DENSE>
 static cudaError_t launch_t(const CUtensorMap &tx, const CUtensorMap &tw, const CUtensorMap &to,
                             const PrefillParams &p, size_t smem, int grid, cudaStream_t s, bool pdl) {
     auto kern = prefill_kernel<DT, ASYM, DENSE>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = raise_smem_cap(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
@@ -713,7 +713,7 @@ cudaError_t prefill_prepare_device(DeviceInfo &dev) {
         prefill_kernel<0, false, false>, prefill_kernel<0, true, false>, prefill_kernel<1, false, false>,
         prefill_kernel<1, true, false>, prefill_kernel<0, false, true>, prefill_kernel<1, false, true>};
     for (auto k : kerns) {
-        const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        const cudaError_t e = raise_smem_cap(reinterpret_cast<const void *>(k), (size_t)smem);
         if (e != cudaSuccess) return e;
     }
     dev.prefill_clusters[0] = 0;
