@@ -229,7 +229,7 @@ def make_sets(w, make, n_sets, shapes_count):
 def run_step(w, layers, outs, only=None):
     for i, (d, o) in enumerate(zip(layers, outs)):
         if only is None or i == only:
-            w.w4a16_gemm(d["x"], d["qweight"], d["scales"], d["qzeros"], d["G"], out=o)
+            w.w4a16_gemm(d["x"], d["qweight"], d["scales"], d["qzeros"], d["G"], out=o, path=d.get("path", 0))
 
 
 class LayerStream:
@@ -540,6 +540,35 @@ def crossover(w, reps=15):
     print(json.dumps({"crossover_largest_decode_m": summary}))
 
 
+def crossover_graph(w, hbm):
+    """Decode vs prefill kernel in the regime the product runs in: each
+    kernel forced, one layer per step, CUDA graphs with programmatic
+    dependent launch, weight sets rotating past L2.  One JSON line per cell
+    and M, then the largest M at which the decode kernel is the faster."""
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size or L2_BYTES_FALLBACK
+    summary = {}
+    for si, (N, K) in enumerate(wl.SWEEP_SHAPES):
+        for (G, sym, dtype) in ((128, True, 1), (32, False, 0)):
+            best_m = 0
+            for M in (1, 2, 4, 6, 8, 12, 16):
+                times = {}
+                for path in ((1, 2) if M <= 8 else (2,)):
+                    d = upload(w, wl.make_problem(M, N, K, G, sym, dtype, seed=8000 + si * 10 + M))
+                    d["path"] = path
+                    st = LayerStream(w, [d], l2, launches_target=32)
+                    times[path] = st.median_step_s(9) * 1e6
+                    del st, d
+                    torch.cuda.empty_cache()
+                if 1 in times and times[1] <= times[2]:
+                    best_m = M
+                print(json.dumps({"crossover_graph_cell": {"N": N, "K": K, "G": G, "sym": sym,
+                                                           "dtype": wl.DTYPE_NAME[dtype], "M": M,
+                                                           "decode_us": None if 1 not in times else round(times[1], 2),
+                                                           "prefill_us": round(times[2], 2)}}), flush=True)
+            summary[f"{N}x{K} G{G} {'sym' if sym else 'asym'} {wl.DTYPE_NAME[dtype]}"] = best_m
+    print(json.dumps({"crossover_graph_largest_decode_m": summary}))
+
+
 def cpu_baseline(sample_steps=None, budget_s=15.0):
     """The oracle (as it stands) on the host cores, on whole decode steps."""
     import oracle
@@ -654,6 +683,8 @@ def main():
                     help="batch size of the --profile-case workload (default: its own)")
     ap.add_argument("--crossover", action="store_true",
                     help="time both kernels at M = 1..16 (the dispatcher's threshold sweep)")
+    ap.add_argument("--crossover-graph", action="store_true",
+                    help="the same comparison in CUDA graphs with early launch and rotating weights")
     ap.add_argument("--cpu-baseline-only", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help=argparse.SUPPRESS)
     args = ap.parse_args()
@@ -693,6 +724,9 @@ def main():
         return
     if args.crossover:
         crossover(w)
+        return
+    if args.crossover_graph:
+        crossover_graph(w, hbm)
         return
 
     l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size or L2_BYTES_FALLBACK
