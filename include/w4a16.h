@@ -27,8 +27,10 @@
  * accumulated in fp32 and rounded once into the output dtype.
  *
  * Ownership: the caller owns every buffer.  Entry points do not allocate,
- * free or synchronise, except w4a16_gemm_host (which synchronises its stream
- * to return the host result).  Per-device state (SM count, kernel attributes,
+ * free or synchronise, except: w4a16_gemm_host synchronises its stream to
+ * return the host result; w4a16_clear_device_error synchronises the device;
+ * the opt-in balanced decode kernel (w4a16_debug_set_config(4)) allocates
+ * its per-stream scratch on the first call that uses it on a stream.  Per-device state (SM count, kernel attributes,
  * the tensor-map encoder) is set up on the first call on each device; make
  * that first call outside stream capture.
  *
@@ -285,6 +287,17 @@ int w4a16_gemm_host(const void *x_host, int M, int K, const int32_t *qweight,
                     const void *scales, const int32_t *qzeros_or_null, int G, int N,
                     void *out_host, w4a16_dtype_t dtype, void *x_dev, void *out_dev,
                     w4a16_stream_t stream);
+
+/* w4a16_gemm_host without the synchronisation: the copy in, the GEMM and
+ * the copy out are enqueued on `stream` and the call returns; out_host holds
+ * y once the stream has reached that point (the caller synchronises, e.g.
+ * once after a whole step of layers).  x_host and out_host must stay valid
+ * and unchanged until then; pinned host memory makes the copies
+ * asynchronous. */
+int w4a16_gemm_host_async(const void *x_host, int M, int K, const int32_t *qweight,
+                          const void *scales, const int32_t *qzeros_or_null, int G, int N,
+                          void *out_host, w4a16_dtype_t dtype, void *x_dev, void *out_dev,
+                          w4a16_stream_t stream);
 
 /* Host-only: which kernel w4a16_gemm would run (W4A16_PATH_DECODE or
  * W4A16_PATH_PREFILL), or a negative status for invalid arguments.  sym != 0

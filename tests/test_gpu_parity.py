@@ -218,6 +218,28 @@ def test_host_buffer_entry_point(cuda_lib):
     assert torch.equal(out_host, ref.cpu())
 
 
+def test_host_buffer_async_entry_point(cuda_lib):
+    """Several layers enqueued through w4a16_gemm_host_async on one stream,
+    one synchronisation: every host result equals the device-buffer call."""
+    w = cuda_lib
+    stream = torch.cuda.Stream()
+    cases = [make_problem(M, N, 512, 64, sym, 1, seed=20 + M) for (M, N, sym) in ((1, 264, True), (4, 520, False),
+                                                                                   (40, 256, True))]
+    devs = [to_device(p, w) for p in cases]
+    xs = [d["x"].cpu().pin_memory() for d in devs]
+    outs = [torch.full((p.M, p.N), 7.0, dtype=torch.bfloat16).pin_memory() for p in cases]
+    dxs = [torch.empty_like(d["x"]) for d in devs]
+    dos = [torch.empty((p.M, p.N), dtype=torch.bfloat16, device="cuda") for p in cases]
+    torch.cuda.synchronize()
+    for p, d, x, o, a, b in zip(cases, devs, xs, outs, dxs, dos):
+        w.w4a16_gemm_host_async(x, d["qweight"], d["scales"], d["qzeros"], p.G, o, a, b, stream=stream)
+    stream.synchronize()
+    for p, d, o in zip(cases, devs, outs):
+        ref = w.w4a16_gemm(d["x"], d["qweight"], d["scales"], d["qzeros"], p.G)
+        torch.cuda.synchronize()
+        assert torch.equal(o, ref.cpu())
+
+
 def test_device_status_clean(cuda_lib):
     torch.cuda.synchronize()
     assert cuda_lib.w4a16_last_device_error() == 0

@@ -27,6 +27,7 @@ from .binding import (  # noqa: F401
     w4a16_gemm_decode_noalloc,
     w4a16_gemm_fused,
     w4a16_gemm_host,
+    w4a16_gemm_host_async,
     w4a16_last_device_error,
     w4a16_moe_gemm,
     w4a16_pack,

@@ -65,6 +65,7 @@ def load_library():
             "w4a16_gemm_dense": [P, I, I, P, I, P, P, I, P],
             "w4a16_gemm_cached": [P, I, I, P, P, P, I, I, P, P, P, I],
             "w4a16_gemm_host": [P, I, I, P, P, P, I, I, P, I, P, P, P],
+            "w4a16_gemm_host_async": [P, I, I, P, P, P, I, I, P, I, P, P, P],
             "w4a16_gemm_decode_noalloc": [P, I, I, P, P, P, I, I, P, P, I],
             "w4a16_select_path": [I, I, I, I, I, I],
             "w4a16_last_device_error": [],
@@ -393,6 +394,18 @@ def w4a16_gemm_host(x_host, qweight, scales, qzeros, G: int, out_host, dev_x, de
     rc = lib.w4a16_gemm_host(_p(x_host), M, K, _p(qweight), _p(scales), _p(qzeros), G, N,
                              _p(out_host), dt, _p(dev_x), _p(dev_out), _stream_ptr(stream))
     _check("w4a16_gemm_host", rc)
+    return out_host
+
+
+def w4a16_gemm_host_async(x_host, qweight, scales, qzeros, G: int, out_host, dev_x, dev_out, stream=None):
+    """w4a16_gemm_host without the synchronisation: copies and GEMM are
+    enqueued on the stream; out_host is valid once the stream is synchronised."""
+    M, K = x_host.shape
+    N = qweight.shape[0]
+    dt = _dtype_code(x_host)
+    rc = load_library().w4a16_gemm_host_async(_p(x_host), M, K, _p(qweight), _p(scales), _p(qzeros), G, N,
+                                              _p(out_host), dt, _p(dev_x), _p(dev_out), _stream_ptr(stream))
+    _check("w4a16_gemm_host_async", rc)
     return out_host
 
 

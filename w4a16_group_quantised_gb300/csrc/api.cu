@@ -347,6 +347,49 @@ int run_gemm(const void *x, int M, int K, const int32_t *qw, const void *scales,
     return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
 }
 
+// Dense-weight GEMM (the dequantised prefill cache) on the prefill kernel.
+int run_gemm_dense(const void *x, int M, int K, const void *w, int N, const void *bias, void *out, int dtype,
+                   w4a16_stream_t stream) {
+    if (dtype != W4A16_F16 && dtype != W4A16_BF16) return W4A16_ERR_DTYPE;
+    if (M < 0 || N <= 0 || K <= 0 || N % 8 != 0 || K % 8 != 0) return W4A16_ERR_SHAPE;
+    if ((long long)M * K >= (1LL << 31) || (long long)N * K >= (1LL << 31) || (long long)M * N >= (1LL << 31))
+        return W4A16_ERR_SHAPE;
+    if (w == nullptr) return W4A16_ERR_NULL;
+    if (M > 0 && (x == nullptr || out == nullptr)) return W4A16_ERR_NULL;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(out)) return W4A16_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(bias) & 1u) != 0) return W4A16_ERR_ALIGN;
+    if (M == 0) return W4A16_OK;
+    const DeviceInfo *dev = nullptr;
+    int rc = get_device(&dev);
+    if (rc != W4A16_OK) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    bool pdl;
+    PrefillCfg c;
+    bool forced;
+    {
+        std::lock_guard<std::mutex> lk(g_cfg_mu);
+        pdl = g_pdl != 0;
+        forced = g_prefill_override;
+        c = g_prefill_cfg;
+    }
+    if (take_weights_written(s)) pdl = false;
+    if (!forced) c = prefill_dense_pick_cfg(M, N, K, *dev);
+    c.wstages = 0;
+    if (!prefill_dense_cfg_valid(c)) return W4A16_ERR_ARG;
+    GemmArgs a{x, nullptr, nullptr, nullptr, out, M, N, K, 0, dtype};
+    a.bias = bias;
+    a.wdense = w;
+    const cudaError_t e = launch_prefill(a, c, *dev, s, pdl);
+    char line[256];
+    std::snprintf(line, sizeof line,
+                  "gemm_dense M=%d N=%d K=%d %s path=prefill kernel=prefill_kernel(dense) BN=%d stages=%d ks=%d "
+                  "pdl=%d bias=%d%s",
+                  M, N, K, dtype == 0 ? "fp16" : "bf16", c.BN, c.stages, c.ks, pdl ? 1 : 0, bias != nullptr ? 1 : 0,
+                  forced ? " (forced)" : "");
+    log_selection(line);
+    return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
+}
+
 }  // namespace
 
 cudaError_t raise_smem_cap(const void *func, size_t need) {
@@ -543,49 +586,6 @@ int w4a16_dequantize(const int32_t *qweight, const void *scales, const int32_t *
     return w4a16_dequant_debug_ex(qweight, scales, qzeros_or_null, G, N, K, w_out, dtype, stream, W4A16_DQ_PREFILL);
 }
 
-namespace {
-int run_gemm_dense(const void *x, int M, int K, const void *w, int N, const void *bias, void *out, int dtype,
-                   w4a16_stream_t stream) {
-    if (dtype != W4A16_F16 && dtype != W4A16_BF16) return W4A16_ERR_DTYPE;
-    if (M < 0 || N <= 0 || K <= 0 || N % 8 != 0 || K % 8 != 0) return W4A16_ERR_SHAPE;
-    if ((long long)M * K >= (1LL << 31) || (long long)N * K >= (1LL << 31) || (long long)M * N >= (1LL << 31))
-        return W4A16_ERR_SHAPE;
-    if (w == nullptr) return W4A16_ERR_NULL;
-    if (M > 0 && (x == nullptr || out == nullptr)) return W4A16_ERR_NULL;
-    if (!aligned16(x) || !aligned16(w) || !aligned16(out)) return W4A16_ERR_ALIGN;
-    if ((reinterpret_cast<uintptr_t>(bias) & 1u) != 0) return W4A16_ERR_ALIGN;
-    if (M == 0) return W4A16_OK;
-    const DeviceInfo *dev = nullptr;
-    int rc = get_device(&dev);
-    if (rc != W4A16_OK) return rc;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    bool pdl;
-    PrefillCfg c;
-    bool forced;
-    {
-        std::lock_guard<std::mutex> lk(g_cfg_mu);
-        pdl = g_pdl != 0;
-        forced = g_prefill_override;
-        c = g_prefill_cfg;
-    }
-    if (take_weights_written(s)) pdl = false;
-    if (!forced) c = prefill_dense_pick_cfg(M, N, K, *dev);
-    c.wstages = 0;
-    if (!prefill_dense_cfg_valid(c)) return W4A16_ERR_ARG;
-    GemmArgs a{x, nullptr, nullptr, nullptr, out, M, N, K, 0, dtype};
-    a.bias = bias;
-    a.wdense = w;
-    const cudaError_t e = launch_prefill(a, c, *dev, s, pdl);
-    char line[256];
-    std::snprintf(line, sizeof line,
-                  "gemm_dense M=%d N=%d K=%d %s path=prefill kernel=prefill_kernel(dense) BN=%d stages=%d ks=%d "
-                  "pdl=%d bias=%d%s",
-                  M, N, K, dtype == 0 ? "fp16" : "bf16", c.BN, c.stages, c.ks, pdl ? 1 : 0, bias != nullptr ? 1 : 0,
-                  forced ? " (forced)" : "");
-    log_selection(line);
-    return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
-}
-}  // namespace
 
 int w4a16_gemm_dense(const void *x, int M, int K, const void *w, int N, const void *bias_or_null, void *out,
                      w4a16_dtype_t dtype, w4a16_stream_t stream) {
@@ -634,9 +634,9 @@ int w4a16_gemm_chain(const void *x, int M, const w4a16_layer_t *layers, int n_la
     return W4A16_OK;
 }
 
-int w4a16_gemm_host(const void *x_host, int M, int K, const int32_t *qweight, const void *scales,
-                    const int32_t *qzeros_or_null, int G, int N, void *out_host, w4a16_dtype_t dtype,
-                    void *x_dev, void *out_dev, w4a16_stream_t stream) {
+int w4a16_gemm_host_async(const void *x_host, int M, int K, const int32_t *qweight, const void *scales,
+                          const int32_t *qzeros_or_null, int G, int N, void *out_host, w4a16_dtype_t dtype,
+                          void *x_dev, void *out_dev, w4a16_stream_t stream) {
     int rc = validate_gemm(x_dev, M, K, qweight, scales, qzeros_or_null, G, N, out_dev, (int)dtype);
     if (rc != W4A16_OK) return rc;
     if (M > 0 && (x_host == nullptr || out_host == nullptr)) return W4A16_ERR_NULL;
@@ -649,7 +649,17 @@ int w4a16_gemm_host(const void *x_host, int M, int K, const int32_t *qweight, co
     if (rc != W4A16_OK) return rc;
     if (cudaMemcpyAsync(out_host, out_dev, (size_t)M * N * 2, cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return W4A16_ERR_CUDA;
-    return cudaStreamSynchronize(s) == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
+    return W4A16_OK;
+}
+
+int w4a16_gemm_host(const void *x_host, int M, int K, const int32_t *qweight, const void *scales,
+                    const int32_t *qzeros_or_null, int G, int N, void *out_host, w4a16_dtype_t dtype,
+                    void *x_dev, void *out_dev, w4a16_stream_t stream) {
+    int rc = w4a16_gemm_host_async(x_host, M, K, qweight, scales, qzeros_or_null, G, N, out_host, dtype, x_dev,
+                                   out_dev, stream);
+    if (rc != W4A16_OK || M == 0) return rc;
+    return cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? W4A16_OK
+                                                                                         : W4A16_ERR_CUDA;
 }
 
 int w4a16_select_path(int M, int N, int K, int G, int sym, int dtype) {
