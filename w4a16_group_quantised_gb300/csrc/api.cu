@@ -560,9 +560,7 @@ int w4a16_moe_gemm(const void *x, int T, int K, const int32_t *qweight, const vo
     }
     if (take_weights_written(s)) pdl = false;
     const bool asym = qzeros_or_null != nullptr;
-    // the configuration of one layer with the rows of every routed slot
-    const int n_all = (int)std::min<long long>(slots * N, 1LL << 30);
-    if (!forced) c = decode_pick_cfg(1, n_all, K, G, !asym, (int)dtype, dev->sm_count, dev->smem_per_sm);
+    if (!forced) c = decode_pick_cfg(1, N, K, G, !asym, (int)dtype, dev->sm_count, dev->smem_per_sm, (int)slots);
     if (!decode_cfg_valid(c, 1, K, G, asym)) return W4A16_ERR_ARG;
     GemmArgs a{x, qweight, scales, qzeros_or_null, out, 1, N, K, G, (int)dtype};
     a.expert_ids = expert_ids;

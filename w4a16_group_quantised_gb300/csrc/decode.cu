@@ -542,22 +542,31 @@ static long long decode_per_sm(const DecodeCfg &c, int M, int K, int G, bool asy
 // row alone can do that): from the base choice, the ring is made as deep as
 // it can be while the grid stays in one wave; failing that, fewer boxes per
 // stage and then more cluster CTAs along K are tried, and the configuration
-// with the fewest waves is kept.
-DecodeCfg decode_pick_cfg(int M, int N, int K, int G, int sym, int dtype, int sm_count, int smem_per_sm) {
+// with the fewest waves is kept.  Larger M (more staged activations and
+// partials per CTA) measured faster with 128-row CTAs; MoE launches (slots > 1
+// expert matrices of the same shape, one token each) have a base of their own.
+DecodeCfg decode_pick_cfg(int M, int N, int K, int G, int sym, int dtype, int sm_count, int smem_per_sm,
+                          int slots) {
     DecodeCfg b;
-    if (N >= 24576)
-        b = DecodeCfg{1, 4, 4, 2, 1};
+    if (slots > 1)                      // MoE: many small expert matrices, one token each
+        b = K <= 1024 ? DecodeCfg{1, 2, 2, 4, 1} : DecodeCfg{1, 4, 4, 4, 2};
+    else if (N >= 24576)
+        b = M >= 3 ? DecodeCfg{1, 8, 1, 4, 2} : DecodeCfg{1, 4, 4, 2, 1};
     else if (N >= 16384)
-        b = DecodeCfg{1, 8, 4, 2, 2};
+        b = (M >= 2 && M <= 5) ? DecodeCfg{1, 8, 2, 3, 2} : DecodeCfg{1, 8, 4, 2, 2};
     else if (N >= 6144)
-        b = K <= 3072 ? DecodeCfg{1, 8, 2, 4, 5} : DecodeCfg{1, 4, 4, 3, 4};
+        b = M >= 2 ? DecodeCfg{1, 8, 4, 2, 5} : (K <= 3072 ? DecodeCfg{1, 8, 2, 4, 5} : DecodeCfg{1, 4, 4, 3, 4});
+    else if (M >= 6 && K >= 8192)
+        b = K >= 12288 ? DecodeCfg{1, 8, 4, 3, 4} : DecodeCfg{1, 8, 4, 4, 6};
+    else if (M >= 3 && K >= 12288)
+        b = DecodeCfg{1, 4, 4, 2, 6};
     else
         b = DecodeCfg{1, 4, 4, 4, 8};
     const bool asym = sym == 0;
     const int nblk = (K + kBoxK - 1) / kBoxK;
     while (b.S > 1 && nblk / b.S < 1) b.S >>= 1;            // at least one K block per CTA
     const int RT = 16 * b.R * b.NW;
-    const long long tiles = (N + RT - 1) / RT;
+    const long long tiles = (long long)((N + RT - 1) / RT) * std::max(slots, 1);
     DecodeCfg best = b;
     long long best_waves = -1;
     for (int S = b.S; S <= 8; S *= 2) {

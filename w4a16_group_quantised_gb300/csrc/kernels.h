@@ -49,7 +49,9 @@ struct DecodeCfg {
     int NS;   // ring stages (2..8)
     int S;    // CTAs along K in a cluster (1..8)
 };
-DecodeCfg decode_pick_cfg(int M, int N, int K, int G, int sym, int dtype, int sm_count, int smem_per_sm);
+// slots > 1: an MoE launch of `slots` expert matrices of N rows each (one token each)
+DecodeCfg decode_pick_cfg(int M, int N, int K, int G, int sym, int dtype, int sm_count, int smem_per_sm,
+                          int slots = 1);
 bool decode_cfg_valid(const DecodeCfg &c, int M, int K, int G, bool asym);
 size_t decode_smem_bytes(const DecodeCfg &c, int M, int K, int G, bool asym);
 // hold_copies: test hook -- the kernel issues no weight copies, so its bounded
