@@ -40,7 +40,6 @@ namespace sk {
 
 constexpr int kUnitK = 128;                          // k per unit
 constexpr int kUnitRows = 16;
-constexpr int kUnitBytes = kUnitRows * kUnitK / 2;   // 1 KB
 constexpr int kNW = 16;                              // warps per CTA
 constexpr int kSlot = 128;                           // floats per partial slot: [16 rows][8 m]
 
