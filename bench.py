@@ -229,7 +229,12 @@ def make_sets(w, make, n_sets, shapes_count):
 def run_step(w, layers, outs, only=None):
     for i, (d, o) in enumerate(zip(layers, outs)):
         if only is None or i == only:
-            w.w4a16_gemm(d["x"], d["qweight"], d["scales"], d["qzeros"], d["G"], out=o, path=d.get("path", 0))
+            if d.get("epi") is not None or d.get("bias") is not None:
+                w.w4a16_gemm_fused(d["x"], d["qweight"], d["scales"], d["qzeros"], d["G"], bias=d.get("bias"),
+                                   epilogue=d.get("epi") or 0, out=o, path=d.get("path", 0))
+            else:
+                w.w4a16_gemm(d["x"], d["qweight"], d["scales"], d["qzeros"], d["G"], out=o,
+                             path=d.get("path", 0))
 
 
 class LayerStream:
@@ -247,7 +252,8 @@ class LayerStream:
         self.n_sets = max(2, int(np.ceil(3 * l2_bytes / self.step_bytes)) + 1)
         self.sets = rotated_sets(base, self.n_sets)
         td = torch.float16 if base[0]["dtype"] == 0 else torch.bfloat16
-        self.outs = [torch.empty((d["M"], d["N"]), dtype=td, device="cuda") for d in base]
+        self.outs = [torch.empty((d["M"], d["N"] // 2 if d.get("epi") == 1 else d["N"]), dtype=td, device="cuda")
+                     for d in base]
         self.stream = torch.cuda.Stream()
         self.chunk = self.n_sets * max(1, launches_target // self.n_sets)
         self.graphs = {}
@@ -377,6 +383,24 @@ def bench_decode_e2e(w, st, steps):
             stream.synchronize()
         dt = (time.perf_counter() - t0) / n
     return dict(dt=dt, h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h, steps=n)
+
+
+def bench_fused_epilogue(w, l2, hbm):
+    """The Qwen3-4B gate_up layer at M = 1 alone, plain, with a bias, and with
+    the fused SiLU-and-multiply (same weights, rotating sets past L2):
+    median microseconds per launch and weight-stream GB/s of each."""
+    name, N, K = wl.QWEN3_4B_SHAPES[2]
+    d0 = upload(w, wl.qwen3_4b_decode(2, 1))
+    bias = torch.randn((N,), generator=torch.Generator().manual_seed(9)).to(torch.bfloat16).cuda()
+    out = {}
+    for tag, extra in (("plain", {}), ("bias", {"bias": bias}), ("silu_mul", {"epi": 1}),
+                       ("bias_silu_mul", {"bias": bias, "epi": 1})):
+        st = LayerStream(w, [dict(d0, **extra)], l2, launches_target=32)
+        t = st.median_step_s(15)
+        out[tag] = {"us": round(t * 1e6, 3), "GB/s": round(st.step_bytes / t / 1e9, 1)}
+        del st
+        torch.cuda.empty_cache()
+    return {"workload": f"qwen3-4b {name} {N}x{K} M=1 bf16 sym G128", **out}
 
 
 def bench_prefill(w, steps, reps=5):
@@ -820,6 +844,7 @@ def main():
         r["TFLOP/s"] = round(sum(2 * 128 * N * K for (_, N, K) in lshapes) / (r["step_us"] * 1e-6) / 1e12, 1)
         extra["prefill_llama31_8b_m128"] = dict(workload="llama-3.1-8b-prefill-m128-asym-g64-bf16", **r)
         extra["moe_decode"] = bench_moe(w, hbm)
+        extra["decode_fused_epilogue"] = bench_fused_epilogue(w, l2, hbm)
         for Mc in (1920, 128):
             rc = bench_prefill_cache(w, Mc, max(2, args.prefill_steps))
             extra[f"prefill_dense_cache_m{Mc}"] = dict(

@@ -87,7 +87,8 @@ typedef enum {
     W4A16_ERR_CUDA = -6,     /* a CUDA runtime call or launch failed          */
     W4A16_ERR_DEVICE = -7,   /* device is not sm_103 / state set-up failed    */
     W4A16_ERR_TIMEOUT = -8,  /* a kernel's bounded wait ran out (device word) */
-    W4A16_ERR_ARG = -9       /* other invalid argument (e.g. path enum)       */
+    W4A16_ERR_ARG = -9       /* other invalid argument (e.g. path enum); in the
+                                device status word: an out-of-range expert id */
 } w4a16_status_t;
 
 /* Concurrency: the default kernels keep no state between calls, so calls on
