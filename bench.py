@@ -475,8 +475,8 @@ def bench_moe(w, hbm, T=1, topk=8, E=128, steps_per_graph=48, reps=20):
     (1536 x 2048) and one over their down (2048 x 768), each step with its own
     seeded routing (a different id buffer per step in the graph), so the
     experts' weights (about 300 MB in all) stream from HBM.  Algorithmic
-    bytes per step: the routed experts' packed weights and scales (each
-    (token, expert) pair counted: a repeated pair is re-read), x and y."""
+    bytes per step: the packed weights and scales of the distinct experts the
+    step routes to (averaged over the steps' routings), x and y."""
     shapes = [("experts gate_up", 1536, 2048), ("experts down", 2048, 768)]
     G = 128
     stacks = []
@@ -488,8 +488,10 @@ def bench_moe(w, hbm, T=1, topk=8, E=128, steps_per_graph=48, reps=20):
         sc = (torch.rand((E, N, K // G), generator=torch.Generator().manual_seed(10 + si)) * 0.018 + 0.002)
         stacks.append(dict(N=N, K=K, qweight=qw, scales=sc.to(torch.bfloat16).cuda()))
     rng = np.random.default_rng(7)
-    ids = [torch.from_numpy(np.stack([rng.choice(E, topk, replace=False) for _ in range(T)]).astype(np.int32)).cuda()
-           for _ in range(steps_per_graph)]
+    ids_h = [np.stack([rng.choice(E, topk, replace=False) for _ in range(T)]).astype(np.int32)
+             for _ in range(steps_per_graph)]
+    ids = [torch.from_numpy(a).cuda() for a in ids_h]
+    distinct = float(np.mean([len(np.unique(a)) for a in ids_h]))   # experts each step must stream
     rw = torch.full((T, topk), 1.0 / topk, dtype=torch.float32, device="cuda")
     x0 = torch.randn((T, shapes[0][2]), generator=torch.Generator().manual_seed(3)).to(torch.bfloat16).cuda()
     x1 = torch.randn((T * topk, shapes[1][2]), generator=torch.Generator().manual_seed(4)).to(torch.bfloat16).cuda()
@@ -521,12 +523,13 @@ def bench_moe(w, hbm, T=1, topk=8, E=128, steps_per_graph=48, reps=20):
             torch.cuda.synchronize()
             ts.append(e0.elapsed_time(e1) / 1e3 / steps_per_graph)
     dt = statistics.median(ts)
-    per_pair = sum(N * K // 2 + N * (K // G) * 2 for (_, N, K) in shapes)
-    step_bytes = T * topk * per_pair + T * shapes[0][2] * 2 + T * topk * (shapes[0][1] + shapes[1][2] + shapes[1][1]) * 2
+    per_expert = sum(N * K // 2 + N * (K // G) * 2 for (_, N, K) in shapes)
+    step_bytes = int(distinct * per_expert) + T * shapes[0][2] * 2 + \
+        T * topk * (shapes[0][1] + shapes[1][2] + shapes[1][1]) * 2
     del stacks, ids, outs
     torch.cuda.empty_cache()
     return {"workload": f"moe-decode T={T} top{topk} of {E} experts, gate_up 1536x2048 + down 2048x768, bf16 sym G128",
-            "step_us": round(dt * 1e6, 3), "GB/s": round(step_bytes / dt / 1e9, 1),
+            "distinct_experts_per_step": round(distinct, 2), "step_us": round(dt * 1e6, 3), "GB/s": round(step_bytes / dt / 1e9, 1),
             "frac": round(step_bytes / dt / 1e9 / hbm, 4), "step_bytes": step_bytes}
 
 
@@ -844,6 +847,7 @@ def main():
         r["TFLOP/s"] = round(sum(2 * 128 * N * K for (_, N, K) in lshapes) / (r["step_us"] * 1e-6) / 1e12, 1)
         extra["prefill_llama31_8b_m128"] = dict(workload="llama-3.1-8b-prefill-m128-asym-g64-bf16", **r)
         extra["moe_decode"] = bench_moe(w, hbm)
+        extra["moe_decode_t4"] = bench_moe(w, hbm, T=4)
         extra["decode_fused_epilogue"] = bench_fused_epilogue(w, l2, hbm)
         for Mc in (1920, 128):
             rc = bench_prefill_cache(w, Mc, max(2, args.prefill_steps))
