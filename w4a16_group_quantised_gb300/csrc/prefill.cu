@@ -119,6 +119,22 @@ __host__ __device__ inline SmemLayout prefill_layout(int BN, int SX, int SA, int
     return L;
 }
 
+// Position in a ring of mbarrier-guarded slots: the slot and the parity of
+// its current phase, advanced by one per use.  (Counters instead of i % S and
+// i / S: with the ring depths as launch parameters those are integer
+// divisions, and on the MMA issuer's and the dequantisers' per-step paths
+// they cost about a fifth of the step.)
+struct RingPos {
+    int slot = 0;
+    uint32_t phase = 0u;
+    __device__ __forceinline__ void next(int depth) {
+        if (++slot == depth) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
 // The epilogue stages a [BN][256] output tile (512 B a row) over the x and A rings.
 __host__ __device__ inline bool prefill_epilogue_fits(int BN, int SX, int SA) {
     return (uint32_t)BN * kBW * 2 <= (uint32_t)SX * BN * 128 + (uint32_t)SA * kATileBytes;
@@ -202,24 +218,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             grid_dependency_wait();  // x may be written by the previous kernel
             const uint32_t xtx = (uint32_t)p.BN * 128u;
-            for (int i = 0; i < nk; ++i) {
-                const int s = i % SX;
-                if (!mbar_wait_bounded(xempty(s), (uint32_t)((i / SX) & 1) ^ 1u, p.status, abort_flag)) break;
-                mbar_arrive_expect_tx(xfull(s), xtx);
-                tma_load_2d(x_base + (uint32_t)s * p.BN * 128u, &tmap_x, xfull(s), (is0 + i) * kBK, m0);
+            RingPos r;
+            for (int i = 0; i < nk; ++i, r.next(SX)) {
+                if (!mbar_wait_bounded(xempty(r.slot), r.phase ^ 1u, p.status, abort_flag)) break;
+                mbar_arrive_expect_tx(xfull(r.slot), xtx);
+                tma_load_2d(x_base + (uint32_t)r.slot * p.BN * 128u, &tmap_x, xfull(r.slot), (is0 + i) * kBK, m0);
             }
         }
     } else if (warp == 3 && DENSE) {
         // ------------------------------------------------------------ dense weight producer
         // 64-k steps of the dtype weight cache straight into the A ring.
         if (lane == 0) {
-            for (int i = 0; i < nk; ++i) {
-                const int a = i % SA;
-                if (!mbar_wait_bounded(aempty(a), (uint32_t)((i / SA) & 1) ^ 1u, p.status, abort_flag)) break;
-                mbar_arrive_expect_tx(afull(a), (uint32_t)kATileBytes);
-                const uint32_t dst = a_base + (uint32_t)a * kATileBytes;
-                tma_load_2d(dst, &tmap_w, afull(a), (is0 + i) * kBK, n0);
-                tma_load_2d(dst + kHalf * 128u, &tmap_w, afull(a), (is0 + i) * kBK, n0 + kHalf);
+            RingPos r;
+            for (int i = 0; i < nk; ++i, r.next(SA)) {
+                if (!mbar_wait_bounded(aempty(r.slot), r.phase ^ 1u, p.status, abort_flag)) break;
+                mbar_arrive_expect_tx(afull(r.slot), (uint32_t)kATileBytes);
+                const uint32_t dst = a_base + (uint32_t)r.slot * kATileBytes;
+                tma_load_2d(dst, &tmap_w, afull(r.slot), (is0 + i) * kBK, n0);
+                tma_load_2d(dst + kHalf * 128u, &tmap_w, afull(r.slot), (is0 + i) * kBK, n0 + kHalf);
             }
         }
     } else if (warp == 3) {
@@ -227,21 +243,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (its own issuing thread: one thread's TMA boxes complete one after another)
         if (lane == 0) {
             const int nw = js1 - js0;
-            for (int j = 0; j < nw; ++j) {
-                const int sw = j % SW;
-                if (!mbar_wait_bounded(wempty(sw), (uint32_t)((j / SW) & 1) ^ 1u, p.status, abort_flag)) break;
-                mbar_arrive_expect_tx(wfull(sw), (uint32_t)kWTileBytes);
-                tma_load_2d(w_base + (uint32_t)sw * kWTileBytes, &tmap_w, wfull(sw), (js0 + j) * (kWK / 8), n0);
+            RingPos r;
+            for (int j = 0; j < nw; ++j, r.next(SW)) {
+                if (!mbar_wait_bounded(wempty(r.slot), r.phase ^ 1u, p.status, abort_flag)) break;
+                mbar_arrive_expect_tx(wfull(r.slot), (uint32_t)kWTileBytes);
+                tma_load_2d(w_base + (uint32_t)r.slot * kWTileBytes, &tmap_w, wfull(r.slot), (js0 + j) * (kWK / 8),
+                            n0);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc = make_idesc_f16(DT, kHalf, p.BN);
-            for (int i = 0; i < nk; ++i) {
-                const int s = i % SX, a = i % SA;
-                if (!mbar_wait_bounded(xfull(s), (uint32_t)((i / SX) & 1), p.status, abort_flag)) break;
-                if (!mbar_wait_bounded(afull(a), (uint32_t)((i / SA) & 1), p.status, abort_flag)) break;
+            RingPos rx, ra;
+            for (int i = 0; i < nk; ++i, rx.next(SX), ra.next(SA)) {
+                const int s = rx.slot, a = ra.slot;
+                if (!mbar_wait_bounded(xfull(s), rx.phase, p.status, abort_flag)) break;
+                if (!mbar_wait_bounded(afull(a), ra.phase, p.status, abort_flag)) break;
                 tc_fence_after();
                 const uint32_t xa = x_base + (uint32_t)s * p.BN * 128u;
                 const uint32_t aa = a_base + (uint32_t)a * kATileBytes;
@@ -347,6 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                sw * 128u;
         const uint32_t w_row = (uint32_t)(r >> 3) * 1024u + sw * 128u;   // packed tile, same swizzle
         const DqConsts dc = p.dq;
+        RingPos rw, ra;                                // packed-weight and A ring positions
         for (int i0 = 0; i0 < nk && ok; i0 += kStepsPerW) {
             unpack_tile_meta();
 #pragma unroll
@@ -359,9 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         zlo = (rz_lo[d] >> zshift) & 0xFu;
                         zhi = (rz_hi[d] >> zshift) & 0xFu;
                     }
-                    const int j = i / kStepsPerW, jj = i % kStepsPerW, swi = j % SW;
-                    if (jj == 0 &&
-                        !mbar_wait_bounded(wfull(swi), (uint32_t)((j / SW) & 1), p.status, abort_flag)) {
+                    const int jj = d, swi = rw.slot;
+                    if (jj == 0 && !mbar_wait_bounded(wfull(swi), rw.phase, p.status, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -379,9 +397,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(wempty(swi));
+                        rw.next(SW);
                     }
-                    const int a = i % SA;
-                    if (!mbar_wait_bounded(aempty(a), (uint32_t)((i / SA) & 1) ^ 1u, p.status, abort_flag)) {
+                    const int a = ra.slot;
+                    const uint32_t aph = ra.phase;
+                    ra.next(SA);
+                    if (!mbar_wait_bounded(aempty(a), aph ^ 1u, p.status, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -521,26 +542,43 @@ static bool prefill_split_fits(const PrefillCfg &c) {
 }
 
 // Time model of one launch (microseconds, fitted to GB300 timings of this
-// kernel): a CTA spends about 3.16 + 0.00175 BN per 256-k packed-weight
-// tile (the dequantisers set the pace up to BN = 256), 5 more for start-up,
-// pipeline fill and epilogue, and, when K is split, 1 + BN / 64 for the
+// kernel over BN x K split x ring depth on the Llama-3.1-8B layers at
+// M = 16...1920, median error 1 %, at most 13 %): a CTA spends about
+// 2.36 + 0.0014 BN per 256-k packed-weight tile, 3.66 more for start-up,
+// pipeline fill and epilogue, and, when K is split, 1.6 + 0.034 BN for the
 // cluster reduction.  CTAs run in waves of what fits on the GPU at once: one
 // CTA per SM, and with a K split whole clusters of KS CTAs, as many as the
-// occupancy query allowed.
+// occupancy query allowed.  (The fit also has 5.5 per launch, the same for
+// every choice, so it is left out.)
 static double prefill_cost(int bn, int ks, long long tiles, int nwt, const DeviceInfo &dev) {
     const int resident = dev.prefill_clusters[ks];
     if (resident <= 0) return 1e30;
     const long long waves = (tiles + resident - 1) / resident;
     const int per_cta = (nwt + ks - 1) / ks;
-    const double t = per_cta * (3.16 + 0.00175 * bn) + 5.0 + (ks > 1 ? 1.0 + bn / 64.0 : 0.0);
+    const double t = per_cta * (2.36 + 0.0014 * bn) + 3.66 + (ks > 1 ? 1.6 + 0.034 * bn : 0.0);
     return (double)waves * t;
 }
 
-// The deepest x ring that fits (with room for the partial tile when K is split).
-static bool prefill_fit_stages(PrefillCfg &c) {
-    for (int sx = 6; sx >= 2; --sx) {
-        c.stages = sx;
-        if (prefill_cfg_fits(c) && (c.ks <= 1 || prefill_split_fits(c))) return true;
+// x beyond this size is streamed from HBM by each wave rather than re-read
+// from L2, so its copies take longer to return.
+constexpr long long kXHotBytes = 32ll << 20;
+
+// Ring depths for a tile: the dequantised-weight (A) ring three deep, so that
+// the dequantisers of a step do not wait for the MMAs of the step before the
+// last, with the deepest x ring that still fits.  An x ring of two is enough
+// only while x stays in L2; for a larger x the A ring stays two deep and the
+// x ring takes the room.  (Measured on the Llama layers: three A stages are
+// 1-7 % faster everywhere except an x ring of two over a 55 MB x, 4-15 %
+// slower.)
+static bool prefill_fit_stages(PrefillCfg &c, long long x_bytes) {
+    for (int sa = 3; sa >= 2; --sa) {
+        c.astages = sa;
+        for (int sx = 6; sx >= 2; --sx) {
+            c.stages = sx;
+            if (!prefill_cfg_fits(c) || (c.ks > 1 && !prefill_split_fits(c))) continue;
+            if (sa == 3 && sx < 3 && x_bytes > kXHotBytes) break;
+            return true;
+        }
     }
     return false;
 }
@@ -563,33 +601,32 @@ static int prefill_best_ks(const PrefillCfg &base, long long tiles, int nwt, con
 }
 
 // Pick BN (tokens per tile, at most M rounded up to 16) and the K split that
-// minimise the modelled time, then the deepest x ring that fits.
+// minimise the modelled time, then the ring depths for that split.
 PrefillCfg prefill_pick_cfg(int M, int N, int K, int G, int sym, int dtype, const DeviceInfo &dev) {
     (void)G; (void)sym; (void)dtype;
     const int ntiles_n = (N + kBW - 1) / kBW;
     const int nwt = (K + kWK - 1) / kWK;
+    const long long xb = (long long)M * K * 2;
     const int bn_max = std::min(256, std::max(16, (M + 15) / 16 * 16));
     PrefillCfg best{bn_max, 2, 2, 2, 1};
     double best_cost = 1e30;
     for (int bn = 16; bn <= bn_max; bn += 16) {
         PrefillCfg c{bn, 2, 2, 2, 1};
-        if (!prefill_fit_stages(c)) continue;
+        if (!prefill_fit_stages(c, xb)) continue;
         const long long tiles = (long long)((M + bn - 1) / bn) * ntiles_n;
         double t = 0.0;
-        c.ks = 1;
-        // the deepest ring that still leaves room for the partial tile
+        // the split needs room for the partial tile over the rings
         PrefillCfg cs = c;
         cs.ks = 2;
-        const bool can_split = prefill_fit_stages(cs);
-        if (can_split) c.stages = cs.stages;
-        c.ks = can_split ? prefill_best_ks(c, tiles, nwt, dev, &t) : 1;
+        const bool can_split = prefill_fit_stages(cs, xb);
+        c.ks = can_split ? prefill_best_ks(cs, tiles, nwt, dev, &t) : 1;
         if (!can_split) t = prefill_cost(bn, 1, tiles, nwt, dev);
         if (t < best_cost * 0.995) {
             best_cost = t;
             best = c;
         }
     }
-    prefill_fit_stages(best);
+    prefill_fit_stages(best, xb);
     return best;
 }
 
