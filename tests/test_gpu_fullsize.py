@@ -50,10 +50,11 @@ def test_llama31_8b_prefill(cuda_lib, shape, M):
     _check(cuda_lib, p, rows=rows)
 
 
-@pytest.mark.parametrize("shape", [2, 3])
+@pytest.mark.parametrize("shape", [0, 2, 3])
 def test_llama31_8b_prefill_repeatable(cuda_lib, shape):
     """Repeated launches on the same inputs give the same bits (the prefill
-    kernel's reduction order is fixed, so any difference is a hazard)."""
+    kernel's reduction order is fixed, so any difference is a hazard).  The
+    qkv shape runs as two launches over two blocks of weight rows."""
     w = cuda_lib
     p = llama31_8b_prefill(shape, 1920)
     d = to_device(p, w)

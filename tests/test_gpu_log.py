@@ -48,3 +48,30 @@ def test_log_every_call(cuda_lib):
     lines = run(2)
     assert len([l for l in lines if "epilogue=none" in l and "path=decode" in l]) == 2
     assert len(run(0)) == 0
+
+
+SPLIT_SCRIPT = r"""
+import sys, torch
+sys.path.insert(0, %r)
+import w4a16_group_quantised_gb300 as w
+w.load_library()
+M, N, K, G = 1920, 6144, 4096, 64
+x = torch.randn(M, K, device="cuda").to(torch.bfloat16)
+qw = torch.randint(-2**31, 2**31 - 1, (N, K // 8), dtype=torch.int32, device="cuda")
+s = (torch.rand(N, K // G, device="cuda") * 0.01 + 0.001).to(torch.bfloat16)
+qz = torch.randint(-2**31, 2**31 - 1, (N // 8, K // G), dtype=torch.int32, device="cuda")
+w.w4a16_gemm(x, qw, s, qz, G)
+torch.cuda.synchronize()
+"""
+
+
+def test_log_prefill_row_split(cuda_lib):
+    """The Llama-3.1-8B qkv layer at M = 1920 (192 wide tiles on 152 SMs)
+    runs as two launches over two blocks of weight rows, and the log says
+    so; the full-size parity test of that layer therefore checks both."""
+    env = dict(os.environ, W4A16_LOG="1")
+    r = subprocess.run([sys.executable, "-c", SPLIT_SCRIPT % ROOT], env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    pre = [l for l in r.stderr.splitlines() if "path=prefill" in l]
+    assert len(pre) == 1 and "rows 0.." in pre[0], pre

@@ -329,19 +329,40 @@ int run_gemm(const void *x, int M, int K, const int32_t *qw, const void *scales,
             log_selection(line);
         }
     } else {
-        PrefillCfg c;
+        PrefillPlan plan;
+        bool forced;
         {
             std::lock_guard<std::mutex> lk(g_cfg_mu);
-            c = g_prefill_override ? g_prefill_cfg
-                                   : prefill_pick_cfg(M, N, K, G, qz == nullptr, dtype, *dev);
+            forced = g_prefill_override;
+            plan.main = plan.tail = g_prefill_cfg;
+            plan.n_split = N;
         }
-        e = launch_prefill(a, c, *dev, s, pdl);
-        char line[320];
-        std::snprintf(line, sizeof line,
-                      "gemm M=%d N=%d K=%d G=%d %s %s path=prefill kernel=prefill_kernel BN=%d x_stages=%d "
-                      "a_stages=%d w_stages=%d ks=%d pdl=%d bias=%d",
-                      M, N, K, G, dtype == 0 ? "fp16" : "bf16", asym ? "asym" : "sym", c.BN, c.stages, c.astages,
-                      c.wstages, c.ks, pdl ? 1 : 0, bias != nullptr ? 1 : 0);
+        if (!forced) plan = prefill_pick_plan(M, N, K, *dev);
+        if (plan.n_split >= N) {
+            e = launch_prefill(a, plan.main, *dev, s, pdl);
+        } else {
+            // rows [0, n_split) in whole waves of wide tiles, then the rest
+            e = launch_prefill(prefill_rows(a, 0, plan.n_split), plan.main, *dev, s, pdl);
+            if (e == cudaSuccess)
+                e = launch_prefill(prefill_rows(a, plan.n_split, N - plan.n_split), plan.tail, *dev, s, pdl);
+        }
+        char line[400];
+        const PrefillCfg &c = plan.main, &t = plan.tail;
+        if (plan.n_split >= N)
+            std::snprintf(line, sizeof line,
+                          "gemm M=%d N=%d K=%d G=%d %s %s path=prefill kernel=prefill_kernel BN=%d x_stages=%d "
+                          "a_stages=%d w_stages=%d ks=%d pdl=%d bias=%d%s",
+                          M, N, K, G, dtype == 0 ? "fp16" : "bf16", asym ? "asym" : "sym", c.BN, c.stages,
+                          c.astages, c.wstages, c.ks, pdl ? 1 : 0, bias != nullptr ? 1 : 0,
+                          forced ? " (forced)" : "");
+        else
+            std::snprintf(line, sizeof line,
+                          "gemm M=%d N=%d K=%d G=%d %s %s path=prefill kernel=prefill_kernel rows 0..%d: BN=%d "
+                          "x_stages=%d a_stages=%d w_stages=%d ks=%d; rows %d..%d: BN=%d x_stages=%d a_stages=%d "
+                          "w_stages=%d ks=%d; pdl=%d bias=%d",
+                          M, N, K, G, dtype == 0 ? "fp16" : "bf16", asym ? "asym" : "sym", plan.n_split, c.BN,
+                          c.stages, c.astages, c.wstages, c.ks, plan.n_split, N, t.BN, t.stages, t.astages, t.wstages,
+                          t.ks, pdl ? 1 : 0, bias != nullptr ? 1 : 0);
         log_selection(line);
     }
     return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;

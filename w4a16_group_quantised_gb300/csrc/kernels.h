@@ -22,6 +22,7 @@ struct GemmArgs {
     const float *route_w = nullptr;
     int n_experts = 0, topk = 0, n_slots = 0;
     int silu_mul = 0;       // 1: out [M, N/2] = silu(y[:, :N/2]) * y[:, N/2:] (rows 0..N/2-1 = gate)
+    int ldo = 0;            // prefill only: elements between output rows (0: N)
 };
 
 // Per-device facts the launchers need.
@@ -101,6 +102,16 @@ bool prefill_dense_cfg_valid(const PrefillCfg &c);
 PrefillCfg prefill_dense_pick_cfg(int M, int N, int K, const DeviceInfo &dev);
 int prefill_dense_best_ks(const PrefillCfg &base, long long tiles, int K, const DeviceInfo &dev, double *cost);
 PrefillCfg prefill_pick_cfg(int M, int N, int K, int G, int sym, int dtype, const DeviceInfo &dev);
+// The fused path's launch plan: weight rows [0, n_split) with `main`, and,
+// when n_split < N, rows [n_split, N) as a second launch with `tail`.
+struct PrefillPlan {
+    PrefillCfg main;
+    int n_split;
+    PrefillCfg tail;
+};
+PrefillPlan prefill_pick_plan(int M, int N, int K, const DeviceInfo &dev);
+// The part of a prefill problem on weight rows [n0, n0 + rows): offset operands, same x and output rows.
+GemmArgs prefill_rows(const GemmArgs &a, int n0, int rows);
 cudaError_t launch_prefill(const GemmArgs &a, const PrefillCfg &c, const DeviceInfo &dev,
                            cudaStream_t s, bool pdl);
 cudaError_t prefill_prepare_device(DeviceInfo &dev);

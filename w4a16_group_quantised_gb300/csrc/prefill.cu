@@ -79,6 +79,7 @@ struct PrefillParams {
     int BN, SX, SA, SW;
     int n_mtiles;
     int KS;               // CTAs of a cluster splitting K (1 = no split)
+    int ldo;              // elements between rows of out (N, or more for a block of columns)
     int *status;
 };
 
@@ -482,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < 8; ++q) peer[q] = cluster.map_shared_rank(part, q < KS ? q : 0);
         const int c_lo = (int)((long long)krank * p.BN / KS), c_hi = (int)((long long)(krank + 1) * p.BN / KS);
         const int n_v = (c_hi - c_lo) * (kBW / 4);      // float4 groups of this CTA's rows
-        const bool vec_out = (p.N & 3) == 0;
+        const bool vec_out = (p.ldo & 3) == 0;
         for (int idx = threadIdx.x; idx < n_v; idx += kThreads) {
             const int c = c_lo + (idx >> 6), nl = (idx & 63) * 4;
             const int m = m0 + c, n = n0 + nl;
@@ -504,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const uint16_t o0 = f32_to_dt16<DT>(sum.x), o1 = f32_to_dt16<DT>(sum.y);
             const uint16_t o2 = f32_to_dt16<DT>(sum.z), o3 = f32_to_dt16<DT>(sum.w);
-            uint16_t *dst = p.out + (size_t)m * p.N + n;
+            uint16_t *dst = p.out + (size_t)m * p.ldo + n;
             if (vec_out && n + 3 < p.N) {
                 *reinterpret_cast<uint2 *>(dst) = make_uint2(o0 | ((uint32_t)o1 << 16), o2 | ((uint32_t)o3 << 16));
             } else {
@@ -628,6 +629,72 @@ PrefillCfg prefill_pick_cfg(int M, int N, int K, int G, int sym, int dtype, cons
     }
     prefill_fit_stages(best, xb);
     return best;
+}
+
+// Per launch, on top of prefill_cost: the constant of the same fit.
+constexpr double kLaunchUs = 5.5;
+
+// Modelled time of one launch with configuration c.
+static double prefill_cfg_cost(const PrefillCfg &c, int M, int N, int K, const DeviceInfo &dev) {
+    const long long tiles = (long long)((M + c.BN - 1) / c.BN) * ((N + kBW - 1) / kBW);
+    return kLaunchUs + prefill_cost(c.BN, std::max(1, c.ks), tiles, (K + kWK - 1) / kWK, dev);
+}
+
+// Wave quantisation: with T tiles on R resident CTAs a last, partly filled
+// wave costs as much as a full one, and a K split needs a partial tile that
+// fits in shared memory (BN <= 208), so it cannot rescue the widest tiles.
+// Each tcgen05 MMA takes about as long at N = 160 as at 256, so narrowing
+// the tiles to even out the waves wastes tensor throughput instead.  The
+// plan may therefore cut the weight rows in two: a first launch of wide
+// tiles (K not split) over the rows that fill whole waves, then the
+// remaining rows as a second launch with the configuration that suits them
+// (often a K split).  The plan with the lower modelled time wins.
+PrefillPlan prefill_pick_plan(int M, int N, int K, const DeviceInfo &dev) {
+    PrefillPlan plan;
+    plan.main = prefill_pick_cfg(M, N, K, 0, 0, 0, dev);
+    plan.n_split = N;
+    plan.tail = plan.main;
+    double best = prefill_cfg_cost(plan.main, M, N, K, dev);
+    const int resident = dev.prefill_clusters[1];
+    const int ntiles_n = (N + kBW - 1) / kBW;
+    const int nwt = (K + kWK - 1) / kWK;
+    const long long xb = (long long)M * K * 2;
+    const int bn_max = std::min(256, std::max(16, (M + 15) / 16 * 16));
+    if (resident <= 0) return plan;
+    for (int bn = 16; bn <= bn_max; bn += 16) {
+        PrefillCfg c{bn, 2, 2, 2, 1};
+        if (!prefill_fit_stages(c, xb)) continue;
+        const int mt = (M + bn - 1) / bn;
+        const int per_wave = resident / mt;            // n-tiles of one full wave
+        if (per_wave <= 0) continue;
+        const int main_nt = (ntiles_n / per_wave) * per_wave;
+        if (main_nt <= 0 || main_nt >= ntiles_n) continue;
+        const int n_split = main_nt * kBW;
+        const PrefillCfg tail = prefill_pick_cfg(M, N - n_split, K, 0, 0, 0, dev);
+        const double t = kLaunchUs + prefill_cost(bn, 1, (long long)main_nt * mt, nwt, dev) +
+                         prefill_cfg_cost(tail, M, N - n_split, K, dev);
+        if (t < best * 0.97) {
+            best = t;
+            plan.main = c;
+            plan.n_split = n_split;
+            plan.tail = tail;
+        }
+    }
+    return plan;
+}
+
+GemmArgs prefill_rows(const GemmArgs &a, int n0, int rows) {
+    GemmArgs b = a;
+    const size_t ng = a.G > 0 ? (size_t)(a.K / a.G) : 0;
+    b.N = rows;
+    b.ldo = a.ldo > 0 ? a.ldo : a.N;
+    b.out = static_cast<uint16_t *>(a.out) + n0;
+    if (a.qweight) b.qweight = a.qweight + (size_t)n0 * (a.K / 8);
+    if (a.scales) b.scales = static_cast<const uint16_t *>(a.scales) + (size_t)n0 * ng;
+    if (a.qzeros) b.qzeros = a.qzeros + (size_t)(n0 / 8) * ng;
+    if (a.bias) b.bias = static_cast<const uint16_t *>(a.bias) + n0;
+    if (a.wdense) b.wdense = static_cast<const uint16_t *>(a.wdense) + (size_t)n0 * a.K;
+    return b;
 }
 
 // ---- dense form (dequantised prefill cache): no packed-weight ring; the x
@@ -815,9 +882,10 @@ cudaError_t launch_prefill(const GemmArgs &a, const PrefillCfg &c, const DeviceI
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
+    const int ldo = a.ldo > 0 ? a.ldo : a.N;
     {
         cuuint64_t dims[2] = {(cuuint64_t)a.N, (cuuint64_t)a.M};
-        cuuint64_t strides[1] = {(cuuint64_t)a.N * 2};
+        cuuint64_t strides[1] = {(cuuint64_t)ldo * 2};
         cuuint32_t box[2] = {(cuuint32_t)kBW, (cuuint32_t)c.BN};
         cuuint32_t estr[2] = {1, 1};
         if (encode(&to, act, 2, a.out, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -833,6 +901,7 @@ cudaError_t launch_prefill(const GemmArgs &a, const PrefillCfg &c, const DeviceI
     p.bias = (const uint16_t *)a.bias;
     p.M = a.M;
     p.N = a.N;
+    p.ldo = ldo;
     p.K = a.K;
     p.G = dense ? 0 : a.G;
     p.ng = dense ? 0 : a.K / a.G;
