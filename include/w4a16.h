@@ -343,10 +343,13 @@ int w4a16_version(void);
  * K), n = 5;
  * which = 2: prefill configuration vals = {BN, x-ring stages, dequantised-
  * weight stages, packed-weight stages[, KS]}, n = 4 or 5 (BN a multiple of
- * 16 in [16, 256]; the rings must fit in shared memory; KS = CTAs of a
- * cluster splitting K, 0 or absent = chosen per call, else 1..8, lowered to
- * the number of 256-k weight tiles; KS > 1 needs the fp32 partial tile,
- * BN KB, to fit over the rings);
+ * 16 in [16, 256]; the rings must fit in shared memory, for the fused
+ * kernel or for the dense form, which has no packed-weight ring and ignores
+ * that entry; KS = CTAs of a cluster splitting K, 0 or absent = chosen per
+ * call, else 1..8, lowered to the number of 256-k weight tiles; KS > 1
+ * needs the fp32 partial tile, BN KB, to fit over the rings).  While set,
+ * every prefill call runs as one launch with it, and a call whose kernel
+ * it does not fit returns W4A16_ERR_ARG;
  * which = 3: programmatic dependent launch on/off, vals = {flag}, n = 1;
  * which = 4: balanced decode kernel vals = {on (1) / off (0), load ring
  * depth in units (2, 4 or 6)}, n = 2;

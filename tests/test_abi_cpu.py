@@ -134,6 +134,8 @@ def test_debug_config_validation(lib):
     assert lib.w4a16_debug_set_config(2, arr, 5) == -9   # more than 8 CTAs
     arr = (ctypes.c_int * 5)(256, 3, 2, 2, 2)
     assert lib.w4a16_debug_set_config(2, arr, 5) == -9   # 256 KB partial tile does not fit
+    arr = (ctypes.c_int * 4)(256, 3, 3, 2)
+    assert lib.w4a16_debug_set_config(2, arr, 4) == 0    # fits the dense form (no packed ring) only
     assert lib.w4a16_debug_set_config(2, None, 0) == 0
     assert lib.w4a16_debug_set_config(9, None, 0) == -9
     assert lib.w4a16_debug_set_config(5, None, 0) == -9   # no such hook

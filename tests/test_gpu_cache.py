@@ -64,6 +64,30 @@ def test_dense_integer_exact_k_split(cuda_lib, ks):
     assert w.w4a16_last_device_error() == 0
 
 
+def test_dense_only_override(cuda_lib):
+    """A forced configuration that fits the dense form only (no room left
+    for the packed-weight ring) runs the dense GEMM, bit-exact on integer
+    data, and the fused GEMM refuses it with W4A16_ERR_ARG."""
+    w = cuda_lib
+    M, N, K, G = 256, 512, 2048, 128
+    p = make_problem(M, N, K, G, False, 1, seed=14300, x_kind="int4")
+    p.scales[:] = 0x3F80
+    d = to_device(p, w)
+    wc = cache_of(w, p, d)
+    w.w4a16_debug_set_config(2, [256, 3, 3, 2])
+    try:
+        out = w.w4a16_gemm_dense(d["x"], wc)
+        torch.cuda.synchronize()
+        with pytest.raises(w.W4A16Error) as ei:
+            w.w4a16_gemm(d["x"], d["qweight"], d["scales"], d["qzeros"], G)
+        assert ei.value.code == -9
+    finally:
+        w.w4a16_debug_set_config(2, None)
+    want = oracle.round_array(oracle.gemm(p.x, M, K, d["ref_qw"], p.scales, d["ref_qz"], G, N, 1), 1)
+    assert np.array_equal(tensor_to_bits(out), want)
+    assert w.w4a16_last_device_error() == 0
+
+
 def test_cached_routing(cuda_lib):
     """Decode-sized M reads int4 (same bits as w4a16_gemm); prefill-sized M
     reads the cache (same bits as w4a16_gemm_dense)."""

@@ -338,6 +338,7 @@ int run_gemm(const void *x, int M, int K, const int32_t *qw, const void *scales,
             plan.n_split = N;
         }
         if (!forced) plan = prefill_pick_plan(M, N, K, *dev);
+        else if (!prefill_cfg_valid(plan.main)) return W4A16_ERR_ARG;   // fits the dense form only
         if (plan.n_split >= N) {
             e = launch_prefill(a, plan.main, *dev, s, pdl);
         } else {
@@ -732,7 +733,9 @@ int w4a16_debug_set_config(int which, const int *vals, int n) {
         if (n == 0) { g_prefill_override = false; return W4A16_OK; }
         if ((n != 4 && n != 5) || vals == nullptr) return W4A16_ERR_ARG;
         PrefillCfg c{vals[0], vals[1], vals[2], vals[3], n == 5 ? vals[4] : 0};
-        if (!prefill_cfg_valid(c)) return W4A16_ERR_ARG;
+        PrefillCfg cd = c;              // the dense form has no packed-weight ring
+        cd.wstages = 0;
+        if (!prefill_cfg_valid(c) && !prefill_dense_cfg_valid(cd)) return W4A16_ERR_ARG;
         g_prefill_cfg = c;
         g_prefill_override = true;
         return W4A16_OK;

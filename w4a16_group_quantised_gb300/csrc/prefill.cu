@@ -745,6 +745,15 @@ int prefill_dense_best_ks(const PrefillCfg &base, long long tiles, int K, const 
     return best;
 }
 
+// The deepest x and A rings (equal depth, at most 4) that fit with c.ks.
+static bool prefill_dense_fit_stages(PrefillCfg &c) {
+    for (int st = 4; st >= 2; --st) {
+        c.stages = c.astages = st;
+        if (prefill_dense_fits(c)) return true;
+    }
+    return false;
+}
+
 PrefillCfg prefill_dense_pick_cfg(int M, int N, int K, const DeviceInfo &dev) {
     const int ntiles_n = (N + kBW - 1) / kBW;
     const int bn_max = std::min(256, std::max(16, (M + 15) / 16 * 16));
@@ -752,21 +761,21 @@ PrefillCfg prefill_dense_pick_cfg(int M, int N, int K, const DeviceInfo &dev) {
     double best_cost = 1e30;
     for (int bn = 16; bn <= bn_max; bn += 16) {
         PrefillCfg c{bn, 2, 2, 0, 1};
-        for (int st = 4; st >= 2; --st) {        // the deepest rings that fit with room for a split
-            c.stages = c.astages = st;
-            c.ks = 2;
-            if (prefill_dense_fits(c)) break;
-        }
-        c.ks = 1;
-        if (!prefill_dense_fits(c)) continue;
+        if (!prefill_dense_fit_stages(c)) continue;
         const long long tiles = (long long)((M + bn - 1) / bn) * ntiles_n;
         double t = 0.0;
-        c.ks = prefill_dense_best_ks(c, tiles, K, dev, &t);
+        // the split needs room for the partial tile over the rings
+        PrefillCfg cs = c;
+        cs.ks = 2;
+        const bool can_split = prefill_dense_fit_stages(cs);
+        c.ks = can_split ? prefill_dense_best_ks(cs, tiles, K, dev, &t) : 1;
+        if (!can_split) t = prefill_dense_cost(bn, 1, tiles, K, dev);
         if (t < best_cost * 0.995) {
             best_cost = t;
             best = c;
         }
     }
+    prefill_dense_fit_stages(best);
     return best;
 }
 
