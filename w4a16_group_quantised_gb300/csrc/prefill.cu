@@ -41,6 +41,11 @@
 //    (r + 1) BN / KS) of the tile (deterministic; KS = 1 is the plain path).
 //    The host picks BN and KS with a time model fitted to this kernel and
 //    the GPU's cluster occupancy.
+//  * Row split: when the wide tiles leave a last wave partly empty, the host
+//    may run the weight rows as two launches -- the rows that fill whole
+//    waves of wide tiles, then the rest with a configuration of their own
+//    (often a K split) -- writing two column blocks of y (out row stride
+//    `ldo`).
 //  * Dense form (the dequantised prefill cache): the weight operand is a
 //    dtype matrix W [N, K] already holding RN((q - z) s); warp 3 loads its
 //    64-k steps (two 128-row boxes, 128-byte swizzle: exactly the canonical
