@@ -556,7 +556,17 @@ DecodeCfg decode_pick_cfg(int M, int N, int K, int G, int sym, int dtype, int sm
         b = (M >= 2 && M <= 5) ? DecodeCfg{1, 8, 2, 3, 2} : DecodeCfg{1, 8, 4, 2, 2};
     else if (N >= 6144)
         b = M >= 2 ? DecodeCfg{1, 8, 4, 2, 5} : (K <= 3072 ? DecodeCfg{1, 8, 2, 4, 5} : DecodeCfg{1, 4, 4, 3, 4});
-    else if (M >= 6 && K >= 8192)
+    else if (M >= 4 && M <= 6 && K >= 12288 && G <= 64) {
+        // Long K with small groups: 128-row CTAs with K over a cluster of 8, or
+        // of 4 when two such CTAs do not fit on an SM (the asymmetric G = 32
+        // slice metadata is large).  Measured on 4096 x 14336 in CUDA graphs
+        // with early launch: G = 64 symmetric 5-9 % faster than the rules
+        // below at M = 4..6, G = 32 asymmetric 4-5 % at M = 4 and 16 % at
+        // M = 5; at M = 3, 7 and 8, and at G = 128, the rules below stay best.
+        b = DecodeCfg{1, 8, 2, 3, 8};
+        const long long ctas8 = (long long)((N + 127) / 128) * 8;
+        if (decode_per_sm(b, M, K, G, sym == 0, dtype, smem_per_sm) * sm_count < ctas8) b.S = 4;
+    } else if (M >= 6 && K >= 8192)
         b = K >= 12288 ? DecodeCfg{1, 8, 4, 3, 4} : DecodeCfg{1, 8, 4, 4, 6};
     else if (M >= 3 && K >= 12288)
         b = DecodeCfg{1, 4, 4, 2, 6};
