@@ -353,12 +353,17 @@ int w4a16_version(void);
  * which = 3: programmatic dependent launch on/off, vals = {flag}, n = 1;
  * which = 4: balanced decode kernel vals = {on (1) / off (0), load ring
  * depth in units (2, 4 or 6)}, n = 2;
+ * which = 8: test of the fused prefill's row split, vals = {n_split}, n = 1
+ * (a positive multiple of 256): every fused prefill call with N > n_split
+ * runs as two launches, weight rows [0, n_split) and [n_split, N), each
+ * with the configuration the dispatcher picks for it (unless which = 2 is
+ * set); n = 0 turns it off;
  * which = 7: test of the timeout path, vals = {on (1) / off (0)}, n = 1:
  * while on, the decode kernel issues no weight copies, so every CTA's bounded
  * wait for them runs out (about 2 s), the kernel leaves without touching
  * memory beyond its own output and records W4A16_ERR_TIMEOUT in the status
  * word (its output is then meaningless); n = 0 turns it off;
- * n = 0 restores the built-in choice for which = 1, 2 or 4.  An invalid
+ * n = 0 restores the built-in choice for which = 1, 2, 4 or 8.  An invalid
  * configuration is rejected here or, for the decode shape limits, by the
  * next w4a16_gemm call with W4A16_ERR_ARG. */
 int w4a16_debug_set_config(int which, const int *vals, int n);

@@ -136,6 +136,12 @@ def test_debug_config_validation(lib):
     assert lib.w4a16_debug_set_config(2, arr, 5) == -9   # 256 KB partial tile does not fit
     arr = (ctypes.c_int * 4)(256, 3, 3, 2)
     assert lib.w4a16_debug_set_config(2, arr, 4) == 0    # fits the dense form (no packed ring) only
+    for bad in (0, -256, 100):                            # row split: a positive multiple of 256
+        arr = (ctypes.c_int * 1)(bad)
+        assert lib.w4a16_debug_set_config(8, arr, 1) == -9
+    arr = (ctypes.c_int * 1)(512)
+    assert lib.w4a16_debug_set_config(8, arr, 1) == 0
+    assert lib.w4a16_debug_set_config(8, None, 0) == 0
     assert lib.w4a16_debug_set_config(2, None, 0) == 0
     assert lib.w4a16_debug_set_config(9, None, 0) == -9
     assert lib.w4a16_debug_set_config(5, None, 0) == -9   # no such hook

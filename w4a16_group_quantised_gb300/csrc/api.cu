@@ -54,6 +54,7 @@ bool g_decode_override = false;
 DecodeCfg g_decode_cfg{};
 bool g_prefill_override = false;
 PrefillCfg g_prefill_cfg{};
+int g_prefill_split = 0;   // > 0: the fused prefill always splits its weight rows there (test hook)
 int g_pdl = 1;
 // Kernel-selection log to stderr (environment W4A16_LOG): 0 off, 1 each
 // distinct selection once, 2 every call.
@@ -331,14 +332,21 @@ int run_gemm(const void *x, int M, int K, const int32_t *qw, const void *scales,
     } else {
         PrefillPlan plan;
         bool forced;
+        int split_at;
         {
             std::lock_guard<std::mutex> lk(g_cfg_mu);
             forced = g_prefill_override;
+            split_at = g_prefill_split;
             plan.main = plan.tail = g_prefill_cfg;
             plan.n_split = N;
         }
         if (!forced) plan = prefill_pick_plan(M, N, K, *dev);
         else if (!prefill_cfg_valid(plan.main)) return W4A16_ERR_ARG;   // fits the dense form only
+        if (!forced && split_at > 0 && split_at < N) {   // test hook: a split where asked, each part picked
+            plan.n_split = split_at;
+            plan.main = prefill_pick_cfg(M, split_at, K, G, qz == nullptr, dtype, *dev);
+            plan.tail = prefill_pick_cfg(M, N - split_at, K, G, qz == nullptr, dtype, *dev);
+        }
         if (plan.n_split >= N) {
             e = launch_prefill(a, plan.main, *dev, s, pdl);
         } else {
@@ -743,6 +751,12 @@ int w4a16_debug_set_config(int which, const int *vals, int n) {
     if (which == 3) {
         if (n != 1 || vals == nullptr) return W4A16_ERR_ARG;
         g_pdl = vals[0] != 0;
+        return W4A16_OK;
+    }
+    if (which == 8) {
+        if (n == 0) { g_prefill_split = 0; return W4A16_OK; }
+        if (n != 1 || vals == nullptr || vals[0] <= 0 || vals[0] % 256 != 0) return W4A16_ERR_ARG;
+        g_prefill_split = vals[0];
         return W4A16_OK;
     }
     if (which == 7) {
