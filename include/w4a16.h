@@ -353,11 +353,11 @@ int w4a16_version(void);
  * which = 3: programmatic dependent launch on/off, vals = {flag}, n = 1;
  * which = 4: balanced decode kernel vals = {on (1) / off (0), load ring
  * depth in units (2, 4 or 6)}, n = 2;
- * which = 8: test of the fused prefill's row split, vals = {n_split}, n = 1
- * (a positive multiple of 256): every fused prefill call with N > n_split
- * runs as two launches, weight rows [0, n_split) and [n_split, N), each
- * with the configuration the dispatcher picks for it (unless which = 2 is
- * set); n = 0 turns it off;
+ * which = 8: test of the prefill row split, vals = {n_split}, n = 1 (a
+ * positive multiple of 256): every prefill call (fused or dense form) with
+ * N > n_split runs as two launches, weight rows [0, n_split) and
+ * [n_split, N), each with the configuration the dispatcher picks for it
+ * (unless which = 2 is set); n = 0 turns it off;
  * which = 7: test of the timeout path, vals = {on (1) / off (0)}, n = 1:
  * while on, the decode kernel issues no weight copies, so every CTA's bounded
  * wait for them runs out (about 2 s), the kernel leaves without touching

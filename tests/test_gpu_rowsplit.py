@@ -8,7 +8,8 @@ through the test hook:
   bias, fp16 and bf16, symmetric and asymmetric, G = 32 / 64 / 128, ragged
   last row blocks;
 * bit-equal to the single launch and to the oracle's rounded sum on
-  integer-exact inputs (s = 1, integer x).
+  integer-exact inputs (s = 1, integer x), for the fused kernel and for the
+  dense form (the dequantised prefill cache).
 """
 import numpy as np
 import pytest
@@ -71,4 +72,32 @@ def test_row_split_integer_exact(cuda_lib, split):
     assert np.array_equal(tensor_to_bits(parts), tensor_to_bits(single))
     want = oracle.round_array(oracle.gemm(p.x, M, K, d["ref_qw"], p.scales, d["ref_qz"], G, N, 1), 1)
     assert np.array_equal(tensor_to_bits(parts), want)
+    assert w.w4a16_last_device_error() == 0
+
+
+@pytest.mark.parametrize("with_bias", [False, True])
+@pytest.mark.parametrize("split", [256, 768])
+def test_dense_row_split(cuda_lib, split, with_bias):
+    """The dense form (the dequantised prefill cache) split the same way:
+    bit-equal to its single launch and to the oracle's rounded sum on
+    integer-exact data, with and without bias."""
+    w = cuda_lib
+    M, N, K, G = 72, 1000, 1024, 128
+    p = make_problem(M, N, K, G, True, 1, seed=15200 + split, x_kind="int4")
+    p.scales[:] = 0x3F80
+    d = to_device(p, w)
+    cache = w.w4a16_dequantize(d["qweight"], d["scales"], d["qzeros"], G)
+    g = torch.Generator().manual_seed(split)
+    bias_t = torch.randint(-8, 9, (N,), generator=g).to(torch.bfloat16).cuda() if with_bias else None
+    single = w.w4a16_gemm_dense(d["x"], cache, bias=bias_t)
+    w.w4a16_debug_set_config(8, [split])
+    try:
+        parts = w.w4a16_gemm_dense(d["x"], cache, bias=bias_t)
+        torch.cuda.synchronize()
+    finally:
+        w.w4a16_debug_set_config(8, None)
+    assert np.array_equal(tensor_to_bits(parts), tensor_to_bits(single))
+    y = oracle.gemm(p.x, M, K, d["ref_qw"], p.scales, d["ref_qz"], G, N, 1)
+    bb = tensor_to_bits(bias_t) if with_bias else None
+    assert np.array_equal(tensor_to_bits(parts), oracle.round_array(oracle.epilogue(y, N, 1, bias=bb), 1))
     assert w.w4a16_last_device_error() == 0

@@ -435,8 +435,8 @@ def w4a16_debug_set_config(which: int, vals=None) -> None:
     {R, NW, NB, NS, S}; which=2 prefill {BN, x stages, A stages, W stages[, KS]};
     which=3 programmatic dependent launch {flag}; which=4 balanced decode
     kernel {on, ring depth}; which=7 timeout-path test {on} (decode kernels
-    issue no weight copies, so their bounded waits run out); which=8 fused
-    prefill row split at {n_split} (a multiple of 256).  vals=None
+    issue no weight copies, so their bounded waits run out); which=8 prefill
+    row split (fused and dense forms) at {n_split} (a multiple of 256).  vals=None
     restores the built-in choice."""
     lib = load_library()
     if vals is None:

@@ -340,7 +340,7 @@ int run_gemm(const void *x, int M, int K, const int32_t *qw, const void *scales,
             plan.main = plan.tail = g_prefill_cfg;
             plan.n_split = N;
         }
-        if (!forced) plan = prefill_pick_plan(M, N, K, *dev);
+        if (!forced) plan = prefill_pick_plan(M, N, K, false, *dev);
         else if (!prefill_cfg_valid(plan.main)) return W4A16_ERR_ARG;   // fits the dense form only
         if (!forced && split_at > 0 && split_at < N) {   // test hook: a split where asked, each part picked
             plan.n_split = split_at;
@@ -394,28 +394,51 @@ int run_gemm_dense(const void *x, int M, int K, const void *w, int N, const void
     if (rc != W4A16_OK) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     bool pdl;
-    PrefillCfg c;
     bool forced;
+    int split_at;
+    PrefillPlan plan;
     {
         std::lock_guard<std::mutex> lk(g_cfg_mu);
         pdl = g_pdl != 0;
         forced = g_prefill_override;
-        c = g_prefill_cfg;
+        split_at = g_prefill_split;
+        plan.main = plan.tail = g_prefill_cfg;
+        plan.n_split = N;
     }
     if (take_weights_written(s)) pdl = false;
-    if (!forced) c = prefill_dense_pick_cfg(M, N, K, *dev);
-    c.wstages = 0;
-    if (!prefill_dense_cfg_valid(c)) return W4A16_ERR_ARG;
+    if (!forced) plan = prefill_pick_plan(M, N, K, true, *dev);
+    if (!forced && split_at > 0 && split_at < N) {   // test hook: a split where asked, each part picked
+        plan.n_split = split_at;
+        plan.main = prefill_dense_pick_cfg(M, split_at, K, *dev);
+        plan.tail = prefill_dense_pick_cfg(M, N - split_at, K, *dev);
+    }
+    plan.main.wstages = plan.tail.wstages = 0;
+    if (!prefill_dense_cfg_valid(plan.main) || !prefill_dense_cfg_valid(plan.tail)) return W4A16_ERR_ARG;
     GemmArgs a{x, nullptr, nullptr, nullptr, out, M, N, K, 0, dtype};
     a.bias = bias;
     a.wdense = w;
-    const cudaError_t e = launch_prefill(a, c, *dev, s, pdl);
-    char line[256];
-    std::snprintf(line, sizeof line,
-                  "gemm_dense M=%d N=%d K=%d %s path=prefill kernel=prefill_kernel(dense) BN=%d stages=%d ks=%d "
-                  "pdl=%d bias=%d%s",
-                  M, N, K, dtype == 0 ? "fp16" : "bf16", c.BN, c.stages, c.ks, pdl ? 1 : 0, bias != nullptr ? 1 : 0,
-                  forced ? " (forced)" : "");
+    cudaError_t e;
+    if (plan.n_split >= N) {
+        e = launch_prefill(a, plan.main, *dev, s, pdl);
+    } else {
+        e = launch_prefill(prefill_rows(a, 0, plan.n_split), plan.main, *dev, s, pdl);
+        if (e == cudaSuccess)
+            e = launch_prefill(prefill_rows(a, plan.n_split, N - plan.n_split), plan.tail, *dev, s, pdl);
+    }
+    const PrefillCfg &c = plan.main, &t = plan.tail;
+    char line[320];
+    if (plan.n_split >= N)
+        std::snprintf(line, sizeof line,
+                      "gemm_dense M=%d N=%d K=%d %s path=prefill kernel=prefill_kernel(dense) BN=%d stages=%d ks=%d "
+                      "pdl=%d bias=%d%s",
+                      M, N, K, dtype == 0 ? "fp16" : "bf16", c.BN, c.stages, c.ks, pdl ? 1 : 0,
+                      bias != nullptr ? 1 : 0, forced ? " (forced)" : "");
+    else
+        std::snprintf(line, sizeof line,
+                      "gemm_dense M=%d N=%d K=%d %s path=prefill kernel=prefill_kernel(dense) rows 0..%d: BN=%d "
+                      "stages=%d ks=%d; rows %d..%d: BN=%d stages=%d ks=%d; pdl=%d bias=%d",
+                      M, N, K, dtype == 0 ? "fp16" : "bf16", plan.n_split, c.BN, c.stages, c.ks, plan.n_split, N,
+                      t.BN, t.stages, t.ks, pdl ? 1 : 0, bias != nullptr ? 1 : 0);
     log_selection(line);
     return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
 }

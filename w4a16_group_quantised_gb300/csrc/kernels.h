@@ -109,7 +109,7 @@ struct PrefillPlan {
     int n_split;
     PrefillCfg tail;
 };
-PrefillPlan prefill_pick_plan(int M, int N, int K, const DeviceInfo &dev);
+PrefillPlan prefill_pick_plan(int M, int N, int K, bool dense, const DeviceInfo &dev);
 // The part of a prefill problem on weight rows [n0, n0 + rows): offset operands, same x and output rows.
 GemmArgs prefill_rows(const GemmArgs &a, int n0, int rows);
 cudaError_t launch_prefill(const GemmArgs &a, const PrefillCfg &c, const DeviceInfo &dev,

@@ -639,10 +639,19 @@ PrefillCfg prefill_pick_cfg(int M, int N, int K, int G, int sym, int dtype, cons
 // Per launch, on top of prefill_cost: the constant of the same fit.
 constexpr double kLaunchUs = 5.5;
 
-// Modelled time of one launch with configuration c.
-static double prefill_cfg_cost(const PrefillCfg &c, int M, int N, int K, const DeviceInfo &dev) {
+static double prefill_dense_cost(int bn, int ks, long long tiles, int K, const DeviceInfo &dev);
+static bool prefill_dense_fit_stages(PrefillCfg &c);
+
+// Modelled time of one launch with configuration c (fused or dense form).
+static double prefill_cfg_cost(const PrefillCfg &c, int M, int N, int K, bool dense, const DeviceInfo &dev) {
     const long long tiles = (long long)((M + c.BN - 1) / c.BN) * ((N + kBW - 1) / kBW);
-    return kLaunchUs + prefill_cost(c.BN, std::max(1, c.ks), tiles, (K + kWK - 1) / kWK, dev);
+    const int ks = std::max(1, c.ks);
+    return kLaunchUs + (dense ? prefill_dense_cost(c.BN, ks, tiles, K, dev)
+                              : prefill_cost(c.BN, ks, tiles, (K + kWK - 1) / kWK, dev));
+}
+
+static PrefillCfg pick_cfg(int M, int N, int K, bool dense, const DeviceInfo &dev) {
+    return dense ? prefill_dense_pick_cfg(M, N, K, dev) : prefill_pick_cfg(M, N, K, 0, 0, 0, dev);
 }
 
 // Wave quantisation: with T tiles on R resident CTAs a last, partly filled
@@ -653,31 +662,31 @@ static double prefill_cfg_cost(const PrefillCfg &c, int M, int N, int K, const D
 // plan may therefore cut the weight rows in two: a first launch of wide
 // tiles (K not split) over the rows that fill whole waves, then the
 // remaining rows as a second launch with the configuration that suits them
-// (often a K split).  The plan with the lower modelled time wins.
-PrefillPlan prefill_pick_plan(int M, int N, int K, const DeviceInfo &dev) {
+// (often a K split).  The plan with the lower modelled time wins.  The
+// same holds for the dense form, with its own configurations and model.
+PrefillPlan prefill_pick_plan(int M, int N, int K, bool dense, const DeviceInfo &dev) {
     PrefillPlan plan;
-    plan.main = prefill_pick_cfg(M, N, K, 0, 0, 0, dev);
+    plan.main = pick_cfg(M, N, K, dense, dev);
     plan.n_split = N;
     plan.tail = plan.main;
-    double best = prefill_cfg_cost(plan.main, M, N, K, dev);
+    double best = prefill_cfg_cost(plan.main, M, N, K, dense, dev);
     const int resident = dev.prefill_clusters[1];
     const int ntiles_n = (N + kBW - 1) / kBW;
-    const int nwt = (K + kWK - 1) / kWK;
     const long long xb = (long long)M * K * 2;
     const int bn_max = std::min(256, std::max(16, (M + 15) / 16 * 16));
     if (resident <= 0) return plan;
     for (int bn = 16; bn <= bn_max; bn += 16) {
-        PrefillCfg c{bn, 2, 2, 2, 1};
-        if (!prefill_fit_stages(c, xb)) continue;
+        PrefillCfg c{bn, 2, 2, dense ? 0 : 2, 1};
+        if (!(dense ? prefill_dense_fit_stages(c) : prefill_fit_stages(c, xb))) continue;
         const int mt = (M + bn - 1) / bn;
         const int per_wave = resident / mt;            // n-tiles of one full wave
         if (per_wave <= 0) continue;
         const int main_nt = (ntiles_n / per_wave) * per_wave;
         if (main_nt <= 0 || main_nt >= ntiles_n) continue;
         const int n_split = main_nt * kBW;
-        const PrefillCfg tail = prefill_pick_cfg(M, N - n_split, K, 0, 0, 0, dev);
-        const double t = kLaunchUs + prefill_cost(bn, 1, (long long)main_nt * mt, nwt, dev) +
-                         prefill_cfg_cost(tail, M, N - n_split, K, dev);
+        const PrefillCfg tail = pick_cfg(M, N - n_split, K, dense, dev);
+        const double t = prefill_cfg_cost(c, M, n_split, K, dense, dev) +
+                         prefill_cfg_cost(tail, M, N - n_split, K, dense, dev);
         if (t < best * 0.97) {
             best = t;
             plan.main = c;
@@ -717,19 +726,19 @@ bool prefill_dense_cfg_valid(const PrefillCfg &c) {
     return prefill_dense_fits(c);
 }
 
-// Time model of the dense form (microseconds): per 64-k step a CTA is bound
-// by the tensor cores (2 x 128 x BN x 64 MACs, about 0.55 BN / 256 us at
-// the measured bf16 rate) or by fetching its operands (32 KB of weights and
-// BN x 128 B of x, about 0.2 us per step from L2 / HBM), plus 4 us of
-// start-up and epilogue and the cluster reduction when K is split.
+// Time model of the dense form (microseconds, fitted to GB300 timings of
+// this kernel over BN x ring depth x K split on the Llama-3.1-8B layers at
+// M = 128 and 1920, median error 3 %): a 64-k step costs 0.376 + 0.00069 BN
+// (nearly the same for any tile width: each MMA costs about the same at any
+// N), plus 3.84 per wave for start-up and epilogue and 1.3 + 0.034 BN for
+// the cluster reduction when K is split.  (The fit also has 5.6 per launch.)
 static double prefill_dense_cost(int bn, int ks, long long tiles, int K, const DeviceInfo &dev) {
     const int resident = dev.prefill_clusters[ks];
     if (resident <= 0) return 1e30;
     const long long waves = (tiles + resident - 1) / resident;
     const int nwt = (K + kWK - 1) / kWK;
     const int steps = ((nwt + ks - 1) / ks) * kStepsPerW;
-    const double step = std::max(0.55 * bn / 256.0, 0.2);
-    return (double)waves * (steps * step + 4.0 + (ks > 1 ? 1.0 + bn / 64.0 : 0.0));
+    return (double)waves * (steps * (0.376 + 0.00069 * bn) + 3.84 + (ks > 1 ? 1.3 + 0.034 * bn : 0.0));
 }
 
 int prefill_dense_best_ks(const PrefillCfg &base, long long tiles, int K, const DeviceInfo &dev, double *cost) {
