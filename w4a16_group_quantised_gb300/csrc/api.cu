@@ -54,7 +54,7 @@ bool g_decode_override = false;
 DecodeCfg g_decode_cfg{};
 bool g_prefill_override = false;
 PrefillCfg g_prefill_cfg{};
-int g_prefill_split = 0;   // > 0: the fused prefill always splits its weight rows there (test hook)
+int g_prefill_split = 0;   // > 0: every prefill call splits its weight rows there (test hook)
 int g_pdl = 1;
 // Kernel-selection log to stderr (environment W4A16_LOG): 0 off, 1 each
 // distinct selection once, 2 every call.
@@ -255,6 +255,17 @@ int select_path_impl(int M, int N, int K, int G, int sym, int dtype) {
     return M <= decode_max_m(N, K, G, sym, dtype) ? W4A16_PATH_DECODE : W4A16_PATH_PREFILL;
 }
 
+// A prefill plan: one launch, or the two row blocks of a split -- rows
+// [0, n_split) in whole waves of wide tiles, then the rest, each writing its
+// columns of y.
+static cudaError_t launch_prefill_plan(const GemmArgs &a, const PrefillPlan &plan, const DeviceInfo &dev,
+                                       cudaStream_t s, bool pdl) {
+    if (plan.n_split >= a.N) return launch_prefill(a, plan.main, dev, s, pdl);
+    cudaError_t e = launch_prefill(prefill_rows(a, 0, plan.n_split), plan.main, dev, s, pdl);
+    if (e == cudaSuccess) e = launch_prefill(prefill_rows(a, plan.n_split, a.N - plan.n_split), plan.tail, dev, s, pdl);
+    return e;
+}
+
 int run_gemm(const void *x, int M, int K, const int32_t *qw, const void *scales, const int32_t *qz,
              int G, int N, void *out, w4a16_stream_t stream, int dtype, int path,
              const void *bias = nullptr, int epilogue = W4A16_EPI_NONE) {
@@ -347,14 +358,7 @@ int run_gemm(const void *x, int M, int K, const int32_t *qw, const void *scales,
             plan.main = prefill_pick_cfg(M, split_at, K, G, qz == nullptr, dtype, *dev);
             plan.tail = prefill_pick_cfg(M, N - split_at, K, G, qz == nullptr, dtype, *dev);
         }
-        if (plan.n_split >= N) {
-            e = launch_prefill(a, plan.main, *dev, s, pdl);
-        } else {
-            // rows [0, n_split) in whole waves of wide tiles, then the rest
-            e = launch_prefill(prefill_rows(a, 0, plan.n_split), plan.main, *dev, s, pdl);
-            if (e == cudaSuccess)
-                e = launch_prefill(prefill_rows(a, plan.n_split, N - plan.n_split), plan.tail, *dev, s, pdl);
-        }
+        e = launch_prefill_plan(a, plan, *dev, s, pdl);
         char line[400];
         const PrefillCfg &c = plan.main, &t = plan.tail;
         if (plan.n_split >= N)
@@ -417,14 +421,7 @@ int run_gemm_dense(const void *x, int M, int K, const void *w, int N, const void
     GemmArgs a{x, nullptr, nullptr, nullptr, out, M, N, K, 0, dtype};
     a.bias = bias;
     a.wdense = w;
-    cudaError_t e;
-    if (plan.n_split >= N) {
-        e = launch_prefill(a, plan.main, *dev, s, pdl);
-    } else {
-        e = launch_prefill(prefill_rows(a, 0, plan.n_split), plan.main, *dev, s, pdl);
-        if (e == cudaSuccess)
-            e = launch_prefill(prefill_rows(a, plan.n_split, N - plan.n_split), plan.tail, *dev, s, pdl);
-    }
+    const cudaError_t e = launch_prefill_plan(a, plan, *dev, s, pdl);
     const PrefillCfg &c = plan.main, &t = plan.tail;
     char line[320];
     if (plan.n_split >= N)
