@@ -136,6 +136,12 @@ def test_debug_config_validation(lib):
     assert lib.w4a16_debug_set_config(2, arr, 5) == -9   # 256 KB partial tile does not fit
     arr = (ctypes.c_int * 4)(256, 3, 3, 2)
     assert lib.w4a16_debug_set_config(2, arr, 4) == 0    # fits the dense form (no packed ring) only
+    arr = (ctypes.c_int * 6)(128, 4, 3, 2, 1, 1)
+    assert lib.w4a16_debug_set_config(2, arr, 6) == 0    # swapped operands at BN = 128
+    arr = (ctypes.c_int * 6)(256, 2, 3, 2, 1, 1)
+    assert lib.w4a16_debug_set_config(2, arr, 6) == -9   # swapped operands need BN = 128
+    arr = (ctypes.c_int * 6)(128, 4, 3, 2, 1, 2)
+    assert lib.w4a16_debug_set_config(2, arr, 6) == -9   # swap flag is 0 or 1
     for bad in (0, -256, 100):                            # row split: a positive multiple of 256
         arr = (ctypes.c_int * 1)(bad)
         assert lib.w4a16_debug_set_config(8, arr, 1) == -9

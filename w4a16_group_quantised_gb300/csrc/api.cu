@@ -364,18 +364,18 @@ int run_gemm(const void *x, int M, int K, const int32_t *qw, const void *scales,
         if (plan.n_split >= N)
             std::snprintf(line, sizeof line,
                           "gemm M=%d N=%d K=%d G=%d %s %s path=prefill kernel=prefill_kernel BN=%d x_stages=%d "
-                          "a_stages=%d w_stages=%d ks=%d pdl=%d bias=%d%s",
+                          "a_stages=%d w_stages=%d ks=%d swap=%d pdl=%d bias=%d%s",
                           M, N, K, G, dtype == 0 ? "fp16" : "bf16", asym ? "asym" : "sym", c.BN, c.stages,
-                          c.astages, c.wstages, c.ks, pdl ? 1 : 0, bias != nullptr ? 1 : 0,
+                          c.astages, c.wstages, c.ks, c.swap, pdl ? 1 : 0, bias != nullptr ? 1 : 0,
                           forced ? " (forced)" : "");
         else
             std::snprintf(line, sizeof line,
                           "gemm M=%d N=%d K=%d G=%d %s %s path=prefill kernel=prefill_kernel rows 0..%d: BN=%d "
-                          "x_stages=%d a_stages=%d w_stages=%d ks=%d; rows %d..%d: BN=%d x_stages=%d a_stages=%d "
-                          "w_stages=%d ks=%d; pdl=%d bias=%d",
+                          "x_stages=%d a_stages=%d w_stages=%d ks=%d swap=%d; rows %d..%d: BN=%d x_stages=%d "
+                          "a_stages=%d w_stages=%d ks=%d swap=%d; pdl=%d bias=%d",
                           M, N, K, G, dtype == 0 ? "fp16" : "bf16", asym ? "asym" : "sym", plan.n_split, c.BN,
-                          c.stages, c.astages, c.wstages, c.ks, plan.n_split, N, t.BN, t.stages, t.astages, t.wstages,
-                          t.ks, pdl ? 1 : 0, bias != nullptr ? 1 : 0);
+                          c.stages, c.astages, c.wstages, c.ks, c.swap, plan.n_split, N, t.BN, t.stages, t.astages,
+                          t.wstages, t.ks, t.swap, pdl ? 1 : 0, bias != nullptr ? 1 : 0);
         log_selection(line);
     }
     return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
@@ -759,8 +759,9 @@ int w4a16_debug_set_config(int which, const int *vals, int n) {
     }
     if (which == 2) {
         if (n == 0) { g_prefill_override = false; return W4A16_OK; }
-        if ((n != 4 && n != 5) || vals == nullptr) return W4A16_ERR_ARG;
-        PrefillCfg c{vals[0], vals[1], vals[2], vals[3], n == 5 ? vals[4] : 0};
+        if ((n < 4 || n > 6) || vals == nullptr) return W4A16_ERR_ARG;
+        PrefillCfg c{vals[0], vals[1], vals[2], vals[3], n >= 5 ? vals[4] : 0};
+        c.swap = n == 6 ? vals[5] : 0;
         PrefillCfg cd = c;              // the dense form has no packed-weight ring
         cd.wstages = 0;
         if (!prefill_cfg_valid(c) && !prefill_dense_cfg_valid(cd)) return W4A16_ERR_ARG;

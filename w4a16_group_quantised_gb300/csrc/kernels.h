@@ -95,6 +95,7 @@ struct PrefillCfg {
     int astages;  // dequantised-weight ring stages
     int wstages;  // packed-weight ring stages (256 k each)
     int ks = 0;   // CTAs of a cluster splitting K: 0 = chosen at launch, else 1..8
+    int swap = 0; // 1: x is the MMA's A operand and the 256 weight rows B (BN must be 128)
 };
 bool prefill_cfg_valid(const PrefillCfg &c);
 // dense form (wdense): no packed-weight ring (wstages unused)

@@ -41,6 +41,10 @@
 //    (r + 1) BN / KS) of the tile (deterministic; KS = 1 is the plain path).
 //    The host picks BN and KS with a time model fitted to this kernel and
 //    the GPU's cluster occupancy.
+//  * Swapped form (128-token tiles): x is the MMA's A operand (M = 128
+//    tokens) and the tile's 256 dequantised weight rows are B (N = 256), one
+//    MMA per 16 k instead of two; TMEM lanes are then tokens, and the
+//    epilogue stages y in four 64-row blocks with a 128-byte swizzle.
 //  * Row split: when the wide tiles leave a last wave partly empty, the host
 //    may run the weight rows as two launches -- the rows that fill whole
 //    waves of wide tiles, then the rest with a configuration of their own
@@ -59,6 +63,7 @@
 #include "ptx.cuh"
 
 #include <algorithm>
+#include <type_traits>
 #include <cooperative_groups.h>
 #include <cuda.h>
 
@@ -85,6 +90,7 @@ struct PrefillParams {
     int n_mtiles;
     int KS;               // CTAs of a cluster splitting K (1 = no split)
     int ldo;              // elements between rows of out (N, or more for a block of columns)
+    int swap;             // 1: x is the MMA's A operand (128 tokens), the weights B (N = 256); BN = 128
     int *status;
 };
 
@@ -260,25 +266,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = make_idesc_f16(DT, kHalf, p.BN);
-            RingPos rx, ra;
-            for (int i = 0; i < nk; ++i, rx.next(SX), ra.next(SA)) {
-                const int s = rx.slot, a = ra.slot;
-                if (!mbar_wait_bounded(xfull(s), rx.phase, p.status, abort_flag)) break;
-                if (!mbar_wait_bounded(afull(a), ra.phase, p.status, abort_flag)) break;
-                tc_fence_after();
-                const uint32_t xa = x_base + (uint32_t)s * p.BN * 128u;
-                const uint32_t aa = a_base + (uint32_t)a * kATileBytes;
+            // Plain: two 128 x BN x 16 MMAs per 16 k (weight halves as A, x as
+            // B).  Swapped (BN = 128): one 128 x 256 x 16 MMA, x as A and all
+            // 256 weight rows as B -- half the instructions for the same tile,
+            // each MMA costing about the same at any N.  The two forms are
+            // separate loops: this thread's instruction stream sets the pace
+            // of the step, and a per-MMA branch measured ~6 % slower.
+            auto issue_steps = [&](auto swap_tag) {
+                constexpr bool SWP = decltype(swap_tag)::value;
+                const uint32_t idesc = SWP ? make_idesc_f16(DT, kHalf, kBW) : make_idesc_f16(DT, kHalf, p.BN);
+                RingPos rx, ra;
+                for (int i = 0; i < nk; ++i, rx.next(SX), ra.next(SA)) {
+                    const int s = rx.slot, a = ra.slot;
+                    if (!mbar_wait_bounded(xfull(s), rx.phase, p.status, abort_flag)) break;
+                    if (!mbar_wait_bounded(afull(a), ra.phase, p.status, abort_flag)) break;
+                    tc_fence_after();
+                    const uint32_t xa = x_base + (uint32_t)s * p.BN * 128u;
+                    const uint32_t aa = a_base + (uint32_t)a * kATileBytes;
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk) {
-                    const uint64_t bdesc = smem_desc_sw128(xa + kk * 32);
-                    const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-                    tc_mma_f16(tmem_d, smem_desc_sw128(aa + kk * 32), bdesc, idesc, acc);
-                    tc_mma_f16(tmem_d + 256u, smem_desc_sw128(aa + kHalf * 128 + kk * 32), bdesc, idesc, acc);
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        const uint64_t xdesc = smem_desc_sw128(xa + kk * 32);
+                        const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                        if constexpr (SWP) {
+                            tc_mma_f16(tmem_d, xdesc, smem_desc_sw128(aa + kk * 32), idesc, acc);
+                        } else {
+                            tc_mma_f16(tmem_d, smem_desc_sw128(aa + kk * 32), xdesc, idesc, acc);
+                            tc_mma_f16(tmem_d + 256u, smem_desc_sw128(aa + kHalf * 128 + kk * 32), xdesc, idesc,
+                                       acc);
+                        }
+                    }
+                    tc_commit(xempty(s));
+                    tc_commit(aempty(a));
                 }
-                tc_commit(xempty(s));
-                tc_commit(aempty(a));
-            }
+            };
+            if (p.swap)
+                issue_steps(std::true_type{});
+            else
+                issue_steps(std::false_type{});
             tc_commit(acc_bar);
         }
         __syncwarp();
@@ -437,7 +461,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (KS > 1) {
             // K split: this CTA's fp32 partial tile -> part[token][weight row]
             // over the (idle) rings; summed across the cluster below.
-            if (have_acc) {
+            if (have_acc && p.swap) {
+                // TMEM lane = token, column = weight row.  Each thread writes 16
+                // consecutive weight rows of its token as four 16-byte chunks,
+                // chunk ch of token row c stored at ch ^ (c % 8) (a quarter-warp
+                // then hits eight different bank groups); the sum below reads
+                // with the same permutation.
+                tc_fence_after();
+                const int q = warp & 3, h = (warp - 4) >> 2;
+                const int c = 32 * q + lane;                          // token row of the tile
+                const uint32_t tbase = tmem_d + ((uint32_t)(32 * q) << 16) + (uint32_t)(h * kHalf);
+                float4 *prow = reinterpret_cast<float4 *>(smem) + (size_t)c * (kBW / 4);
+                for (int c0 = 0; c0 < kHalf; c0 += 16) {
+                    uint32_t v[16];
+                    tmem_ld_32x32b_x16(tbase + (uint32_t)c0, v);
+                    const int ch0 = (h * kHalf + c0) >> 2;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        prow[(ch0 + u) ^ (c & 7)] = make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
+                                                                __uint_as_float(v[4 * u + 2]),
+                                                                __uint_as_float(v[4 * u + 3]));
+                }
+            } else if (have_acc) {
                 tc_fence_after();
                 const int q = warp & 3, h = (warp - 4) >> 2;
                 const int nl = h * kHalf + 32 * q + lane;
@@ -451,7 +496,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         } else {
-            if (have_acc) {
+            if (have_acc && p.swap) {
+                // TMEM lane = token, column = weight row.  The tile is staged as
+                // four blocks of 64 weight rows, [BN tokens][128 B] each in the
+                // 128-byte-swizzled layout of the store map (16-byte chunk ch of
+                // token row c at ch ^ (c % 8)), and leaves in four TMA stores.
+                tc_fence_after();
+                const int q = warp & 3, h = (warp - 4) >> 2;
+                const int c = 32 * q + lane;                          // token row of the tile
+                const uint32_t tbase = tmem_d + ((uint32_t)(32 * q) << 16) + (uint32_t)(h * kHalf);
+                for (int c0 = 0; c0 < kHalf; c0 += 16) {
+                    uint32_t v[16];
+                    tmem_ld_32x32b_x16(tbase + (uint32_t)c0, v);
+                    const int col = h * kHalf + c0;                   // first weight row of the 16
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        float a = __uint_as_float(v[2 * u]), b = __uint_as_float(v[2 * u + 1]);
+                        if (p.bias != nullptr) {
+                            const int n = n0 + col + 2 * u;
+                            if (n < p.N) a += dt16_to_f32<DT>(__ldg(p.bias + n));
+                            if (n + 1 < p.N) b += dt16_to_f32<DT>(__ldg(p.bias + n + 1));
+                        }
+                        pk[u] = (uint32_t)f32_to_dt16<DT>(a) | ((uint32_t)f32_to_dt16<DT>(b) << 16);
+                    }
+                    unsigned char *blk = smem + (size_t)(col >> 6) * ((size_t)p.BN * 128) + (size_t)c * 128;
+                    const int ch = (col & 63) >> 3;                   // two 16-byte chunks of 8 weight rows
+                    *reinterpret_cast<uint4 *>(blk + (((ch) ^ (c & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    *reinterpret_cast<uint4 *>(blk + (((ch + 1) ^ (c & 7)) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                }
+                fence_proxy_async_smem();
+            } else if (have_acc) {
                 tc_fence_after();
                 const int q = warp & 3, h = (warp - 4) >> 2;
                 const int nl = h * kHalf + 32 * q + lane;            // row of the tile
@@ -469,7 +544,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             named_barrier_sync(1, kDeqWarps * 32);
             if (have_acc && threadIdx.x == 128) {
-                tma_store_2d(&tmap_out, smem_u32(smem), n0, m0);
+                if (p.swap) {
+                    for (int b = 0; b < kBW / 64; ++b)
+                        if (n0 + 64 * b < p.N)   // boxes wholly past the last weight row are not issued
+                            tma_store_2d(&tmap_out, smem_u32(smem) + (uint32_t)(b * p.BN * 128), n0 + 64 * b, m0);
+                } else {
+                    tma_store_2d(&tmap_out, smem_u32(smem), n0, m0);
+                }
                 bulk_commit_group();
                 bulk_wait_group_all();
             }
@@ -493,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int c = c_lo + (idx >> 6), nl = (idx & 63) * 4;
             const int m = m0 + c, n = n0 + nl;
             if (m >= p.M || n >= p.N) continue;
-            const size_t off = (size_t)c * kBW + nl;
+            const size_t off = (size_t)c * kBW + (p.swap ? (size_t)((((nl >> 2) ^ (c & 7))) << 2) : (size_t)nl);
             float4 sum = *reinterpret_cast<const float4 *>(peer[0] + off);
 #pragma unroll
             for (int q = 1; q < 8; ++q) {
@@ -633,6 +714,10 @@ PrefillCfg prefill_pick_cfg(int M, int N, int K, int G, int sym, int dtype, cons
         }
     }
     prefill_fit_stages(best, xb);
+    // 128-token tiles run with swapped operands where that measured faster
+    // (5-10 % at a K split of 1 to 3 on the Llama layers at M = 16..1920;
+    // mixed at 4 and more).
+    if (best.BN == kHalf && best.ks <= 3) best.swap = 1;
     return best;
 }
 
@@ -678,6 +763,7 @@ PrefillPlan prefill_pick_plan(int M, int N, int K, bool dense, const DeviceInfo 
     for (int bn = 16; bn <= bn_max; bn += 16) {
         PrefillCfg c{bn, 2, 2, dense ? 0 : 2, 1};
         if (!(dense ? prefill_dense_fit_stages(c) : prefill_fit_stages(c, xb))) continue;
+        if (!dense && bn == kHalf) c.swap = 1;
         const int mt = (M + bn - 1) / bn;
         const int per_wave = resident / mt;            // n-tiles of one full wave
         if (per_wave <= 0) continue;
@@ -721,6 +807,7 @@ static bool prefill_dense_fits(const PrefillCfg &c) {
 
 bool prefill_dense_cfg_valid(const PrefillCfg &c) {
     if (c.BN < 16 || c.BN > 256 || c.BN % 16 != 0) return false;
+    if (c.swap != 0 && (c.swap != 1 || c.BN != kHalf)) return false;
     if (c.stages < 2 || c.astages < 2) return false;
     if (c.ks < 0 || c.ks > 8) return false;
     return prefill_dense_fits(c);
@@ -795,6 +882,7 @@ PrefillCfg prefill_dense_pick_cfg(int M, int N, int K, const DeviceInfo &dev) {
 
 bool prefill_cfg_valid(const PrefillCfg &c) {
     if (c.BN < 16 || c.BN > 256 || c.BN % 16 != 0) return false;
+    if (c.swap != 0 && (c.swap != 1 || c.BN != kHalf)) return false;
     if (c.stages < 2 || c.astages < 2 || c.wstages < 2) return false;
     if (c.ks < 0 || c.ks > 8) return false;
     if (c.ks > 1 && !prefill_split_fits(c)) return false;
@@ -907,12 +995,13 @@ cudaError_t launch_prefill(const GemmArgs &a, const PrefillCfg &c, const DeviceI
     }
     const int ldo = a.ldo > 0 ? a.ldo : a.N;
     {
+        // plain: one [BN][256] box; swapped: [BN][64] boxes, 128-byte swizzle
         cuuint64_t dims[2] = {(cuuint64_t)a.N, (cuuint64_t)a.M};
         cuuint64_t strides[1] = {(cuuint64_t)ldo * 2};
-        cuuint32_t box[2] = {(cuuint32_t)kBW, (cuuint32_t)c.BN};
+        cuuint32_t box[2] = {(cuuint32_t)(c.swap ? 64 : kBW), (cuuint32_t)c.BN};
         cuuint32_t estr[2] = {1, 1};
         if (encode(&to, act, 2, a.out, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   c.swap ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
@@ -925,6 +1014,7 @@ cudaError_t launch_prefill(const GemmArgs &a, const PrefillCfg &c, const DeviceI
     p.M = a.M;
     p.N = a.N;
     p.ldo = ldo;
+    p.swap = c.swap ? 1 : 0;
     p.K = a.K;
     p.G = dense ? 0 : a.G;
     p.ng = dense ? 0 : a.K / a.G;
