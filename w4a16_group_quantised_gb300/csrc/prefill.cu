@@ -131,6 +131,61 @@ __host__ __device__ inline SmemLayout prefill_layout(int BN, int SX, int SA, int
     return L;
 }
 
+// One 64-k step of MMAs from descriptor words.  The issuing thread's
+// instruction stream sets the pace of a step, so the descriptors are built
+// once per step rather than per MMA (about 1 % on the Llama layers at
+// M >= 512): the low word of a shared-memory descriptor (smem_desc_sw128)
+// is (address >> 4) plus fixed fields, so the 16-k slice kk of a 128-byte-
+// swizzled operand is lo + 2 kk, and the high word is the same for every
+// operand.  first = 0 starts a fresh accumulation with the step's first MMA
+// (predicate p); the others accumulate (predicate q, true because an
+// instruction descriptor is never zero).
+// tc_mma8: the plain form, weight halves a0 / a1 (A) against x (B), into
+// the accumulators at d and d + 256.
+__device__ __forceinline__ void tc_mma8(uint32_t d, uint32_t a0lo, uint32_t a1lo, uint32_t blo, uint32_t hi,
+                                        uint32_t idesc, uint32_t first) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t.reg .b64 a, b;\n\t.reg .b32 t;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+        "mov.b64 a, {%1, %4};\n\tmov.b64 b, {%3, %4};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, p;\n\t"
+        "mov.b64 a, {%2, %4};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%7], a, b, %5, p;\n\t"
+        "add.u32 t, %1, 2;\n\tmov.b64 a, {t, %4};\n\tadd.u32 t, %3, 2;\n\tmov.b64 b, {t, %4};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, q;\n\t"
+        "add.u32 t, %2, 2;\n\tmov.b64 a, {t, %4};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%7], a, b, %5, q;\n\t"
+        "add.u32 t, %1, 4;\n\tmov.b64 a, {t, %4};\n\tadd.u32 t, %3, 4;\n\tmov.b64 b, {t, %4};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, q;\n\t"
+        "add.u32 t, %2, 4;\n\tmov.b64 a, {t, %4};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%7], a, b, %5, q;\n\t"
+        "add.u32 t, %1, 6;\n\tmov.b64 a, {t, %4};\n\tadd.u32 t, %3, 6;\n\tmov.b64 b, {t, %4};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, q;\n\t"
+        "add.u32 t, %2, 6;\n\tmov.b64 a, {t, %4};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%7], a, b, %5, q;\n\t}"
+        ::"r"(d), "r"(a0lo), "r"(a1lo), "r"(blo), "r"(hi), "r"(idesc), "r"(first), "r"(d + 256u)
+        : "memory");
+}
+
+// tc_mma4_swp: the swapped form, x (A, 128 tokens) against all 256 weight
+// rows (B), into the accumulator at d.
+__device__ __forceinline__ void tc_mma4_swp(uint32_t d, uint32_t xlo, uint32_t wlo, uint32_t hi, uint32_t idesc,
+                                            uint32_t first) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t.reg .b64 a, b;\n\t.reg .b32 t;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\tsetp.ne.b32 q, %4, 0;\n\t"
+        "mov.b64 a, {%1, %3};\n\tmov.b64 b, {%2, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, p;\n\t"
+        "add.u32 t, %1, 2;\n\tmov.b64 a, {t, %3};\n\tadd.u32 t, %2, 2;\n\tmov.b64 b, {t, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, q;\n\t"
+        "add.u32 t, %1, 4;\n\tmov.b64 a, {t, %3};\n\tadd.u32 t, %2, 4;\n\tmov.b64 b, {t, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, q;\n\t"
+        "add.u32 t, %1, 6;\n\tmov.b64 a, {t, %3};\n\tadd.u32 t, %2, 6;\n\tmov.b64 b, {t, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, q;\n\t}"
+        ::"r"(d), "r"(xlo), "r"(wlo), "r"(hi), "r"(idesc), "r"(first)
+        : "memory");
+}
+
 // Position in a ring of mbarrier-guarded slots: the slot and the parity of
 // its current phase, advanced by one per use.  (Counters instead of i % S and
 // i / S: with the ring depths as launch parameters those are integer
@@ -275,6 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto issue_steps = [&](auto swap_tag) {
                 constexpr bool SWP = decltype(swap_tag)::value;
                 const uint32_t idesc = SWP ? make_idesc_f16(DT, kHalf, kBW) : make_idesc_f16(DT, kHalf, p.BN);
+                const uint32_t dlo0 = (uint32_t)smem_desc_sw128(0u), dhi = (uint32_t)(smem_desc_sw128(0u) >> 32);
                 RingPos rx, ra;
                 for (int i = 0; i < nk; ++i, rx.next(SX), ra.next(SA)) {
                     const int s = rx.slot, a = ra.slot;
@@ -283,16 +339,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     const uint32_t xa = x_base + (uint32_t)s * p.BN * 128u;
                     const uint32_t aa = a_base + (uint32_t)a * kATileBytes;
-#pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        const uint64_t xdesc = smem_desc_sw128(xa + kk * 32);
-                        const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                    {
+                        const uint32_t xlo = dlo0 + (xa >> 4), alo = dlo0 + (aa >> 4);
+                        const uint32_t first = i > 0 ? 1u : 0u;
                         if constexpr (SWP) {
-                            tc_mma_f16(tmem_d, xdesc, smem_desc_sw128(aa + kk * 32), idesc, acc);
+                            tc_mma4_swp(tmem_d, xlo, alo, dhi, idesc, first);
                         } else {
-                            tc_mma_f16(tmem_d, smem_desc_sw128(aa + kk * 32), xdesc, idesc, acc);
-                            tc_mma_f16(tmem_d + 256u, smem_desc_sw128(aa + kHalf * 128 + kk * 32), xdesc, idesc,
-                                       acc);
+                            tc_mma8(tmem_d, alo, alo + (uint32_t)(kHalf * 128 / 16), xlo, dhi, idesc, first);
                         }
                     }
                     tc_commit(xempty(s));
