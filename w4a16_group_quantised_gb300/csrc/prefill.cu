@@ -448,6 +448,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                sw * 128u;
         const uint32_t w_row = (uint32_t)(r >> 3) * 1024u + sw * 128u;   // packed tile, same swizzle
         const DqConsts dc = p.dq;
+        // G >= 64: both 32-k halves of a step are in one group, so its constants
+        // are built once (the dequantisers share the SM's issue slots with the
+        // MMA issuer: 1-2.5 % on the Llama layers at M = 1920).
+        const int one_group = gcount <= 4 ? 1 : 0;
         RingPos rw, ra;                                // packed-weight and A ring positions
         for (int i0 = 0; i0 < nk && ok; i0 += kStepsPerW) {
             unpack_tile_meta();
@@ -455,12 +459,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int d = 0; d < kStepsPerW; ++d) {
                 const int i = i0 + d;
                 if (i < nk && ok) {
-                    const uint32_t slo = rs_lo[d], shi = rs_hi[d];
-                    uint32_t zlo = 8u, zhi = 8u;
-                    if (ASYM) {
-                        zlo = (rz_lo[d] >> zshift) & 0xFu;
-                        zhi = (rz_hi[d] >> zshift) & 0xFu;
-                    }
+                    const uint32_t slo = rs_lo[d];
+                    uint32_t zlo = 8u;
+                    if (ASYM) zlo = (rz_lo[d] >> zshift) & 0xFu;
                     const int jj = d, swi = rw.slot;
                     if (jj == 0 && !mbar_wait_bounded(wfull(swi), rw.phase, p.status, abort_flag)) {
                         ok = false;
@@ -489,8 +490,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    const uint32_t zc_lo = zseq2<DT>(zlo), zc_hi = zseq2<DT>(zhi);
-                    const uint32_t s2lo = rep2(slo), s2hi = rep2(shi);
+                    const uint32_t zc_lo = zseq2<DT>(zlo), s2lo = rep2(slo);
+                    uint32_t zc_hi = zc_lo, s2hi = s2lo;
+                    if (one_group == 0) {        // G = 32: the step's two halves have their own group
+                        zc_hi = zseq2<DT>(ASYM ? (rz_hi[d] >> zshift) & 0xFu : 8u);
+                        s2hi = rep2(rs_hi[d]);
+                    }
                     unsigned char *adst = smem + L.a_off + (size_t)a * kATileBytes + a_row;
                     const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
