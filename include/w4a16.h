@@ -305,6 +305,18 @@ int w4a16_gemm_host_async(const void *x_host, int M, int K, const int32_t *qweig
  * means qzeros_or_null == NULL. */
 int w4a16_select_path(int M, int N, int K, int G, int sym, int dtype);
 
+/* Test hook: the prefill launch plan the dispatcher would pick for an
+ * M x N x K problem (dense != 0: the dense form) on a device with sm_count
+ * SMs whose prefill kernel keeps clusters[k - 1] clusters of k CTAs resident
+ * at once (k = 1..8, as the occupancy query reports).  Host arithmetic only:
+ * no device is touched.  out (13 ints, caller-owned) receives n_split (N
+ * when the plan is one launch), then for the first and the second launch
+ * {BN, x-ring stages, dequantised-weight stages, packed-weight stages, KS,
+ * swapped operands (0/1)}.  Returns W4A16_OK, or W4A16_ERR_ARG for a
+ * non-positive or misaligned shape, sm_count <= 0, a negative cluster count
+ * or a NULL pointer. */
+int w4a16_debug_prefill_plan(int M, int N, int K, int dense, int sm_count, const int *clusters, int *out);
+
 /* The decode GEMM (M <= 8) without any device allocation, ever.  The pages
  * have no counterpart of this entry point: it is a library addition for
  * callers that must not allocate device memory after start-up (an engine

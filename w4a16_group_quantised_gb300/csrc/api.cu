@@ -716,6 +716,31 @@ int w4a16_select_path(int M, int N, int K, int G, int sym, int dtype) {
     return select_path_impl(M, N, K, G, sym != 0, dtype);
 }
 
+int w4a16_debug_prefill_plan(int M, int N, int K, int dense, int sm_count, const int *clusters, int *out) {
+    if (M <= 0 || N <= 0 || K <= 0 || N % 8 != 0 || K % 8 != 0 || sm_count <= 0 || clusters == nullptr ||
+        out == nullptr)
+        return W4A16_ERR_ARG;
+    DeviceInfo dev{};
+    dev.sm_count = sm_count;
+    dev.prefill_clusters[0] = 0;
+    for (int k = 1; k <= 8; ++k) {
+        if (clusters[k - 1] < 0) return W4A16_ERR_ARG;
+        dev.prefill_clusters[k] = clusters[k - 1];
+    }
+    const PrefillPlan plan = prefill_pick_plan(M, N, K, dense != 0, dev);
+    const PrefillCfg *cs[2] = {&plan.main, &plan.tail};
+    out[0] = plan.n_split;
+    for (int i = 0; i < 2; ++i) {
+        out[1 + 6 * i] = cs[i]->BN;
+        out[2 + 6 * i] = cs[i]->stages;
+        out[3 + 6 * i] = cs[i]->astages;
+        out[4 + 6 * i] = cs[i]->wstages;
+        out[5 + 6 * i] = cs[i]->ks;
+        out[6 + 6 * i] = cs[i]->swap;
+    }
+    return W4A16_OK;
+}
+
 int w4a16_last_device_error(void) {
     const DeviceInfo *dev = nullptr;
     int rc = get_device(&dev);
