@@ -628,6 +628,46 @@ def crossover_graph(w, hbm):
     print(json.dumps({"crossover_graph_largest_decode_m": summary}))
 
 
+def decode_timeline(w, reps=3):
+    """Where one M = 1 decode step goes: the benchmark's graphed step of the
+    four Qwen3-4B-shaped layers (rotating weight sets, early launch) on the
+    trace build of the library (libw4a16_trace.so: the decode kernel with its
+    timeline stamps compiled in) with the hook on.  After each of `reps`
+    graph replays, per layer: the min / median / max over CTAs of entry,
+    release (grid dependency wait returned), first weight stage ready and
+    exit, the median loop time and the tail (last minus median exit), in
+    microseconds from the step's first CTA entry.  One JSON line per replay."""
+    shapes = wl.QWEN3_4B_SHAPES
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size or L2_BYTES_FALLBACK
+    base = [upload(w, wl.qwen3_4b_decode(i, 1)) for i in range(len(shapes))]
+    st = LayerStream(w, base, l2, launches_target=32)
+    buf = w.w4a16_debug_decode_trace([(N, K) for (_, N, K) in shapes])
+    try:
+        for rep in range(reps):
+            st.replay_steps(st.chunk)
+            torch.cuda.synchronize()
+            tr = buf.cpu().numpy()
+            used = tr[:, :, 0] > 0
+            t0 = tr[:, :, 0][used].min()
+            q = lambda v: [round(float(v.min()), 2), round(float(np.median(v)), 2), round(float(v.max()), 2)]
+            out, prev_exit = {}, None
+            for li, (name, N, K) in enumerate(shapes):
+                a = (tr[li][used[li]].astype(np.int64) - t0) / 1000.0
+                d = {"ctas": int(a.shape[0]), "entry": q(a[:, 0]), "released": q(a[:, 1]),
+                     "first_stage": q(a[:, 3]), "exit": q(a[:, 6]),
+                     "loop_us_median": round(float(np.median(a[:, 4] - a[:, 3])), 2),
+                     "tail_us": round(float(a[:, 6].max() - np.median(a[:, 6])), 2)}
+                if prev_exit is not None:
+                    d["release_after_previous_last_exit_us"] = round(float(a[:, 1].min() - prev_exit), 2)
+                prev_exit = float(a[:, 6].max())
+                out[name] = d
+            print(json.dumps({"decode_timeline": out, "replay": rep}), flush=True)
+    finally:
+        w.w4a16_debug_decode_trace(None)
+        del buf, st, base
+        torch.cuda.empty_cache()
+
+
 def cpu_baseline(sample_steps=None, budget_s=15.0):
     """The oracle (as it stands) on the host cores, on whole decode steps."""
     import oracle
@@ -744,6 +784,8 @@ def main():
                     help="time both kernels at M = 1..16 (the dispatcher's threshold sweep)")
     ap.add_argument("--crossover-graph", action="store_true",
                     help="the same comparison in CUDA graphs with early launch and rotating weights")
+    ap.add_argument("--decode-timeline", action="store_true",
+                    help="per-CTA timeline of one graphed M=1 decode step (builds and loads the trace build)")
     ap.add_argument("--cpu-baseline-only", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help=argparse.SUPPRESS)
     args = ap.parse_args()
@@ -774,7 +816,11 @@ def main():
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
     from w4a16_group_quantised_gb300 import build as libbuild
-    libbuild.build()
+    if args.decode_timeline:                         # the profiling build, stamps compiled in
+        os.environ["W4A16_LIBRARY"] = "trace"
+        libbuild.build(variant="trace")
+    else:
+        libbuild.build()
     import w4a16_group_quantised_gb300 as w
     w.load_library()
 
@@ -786,6 +832,9 @@ def main():
         return
     if args.crossover_graph:
         crossover_graph(w, hbm)
+        return
+    if args.decode_timeline:
+        decode_timeline(w)
         return
 
     l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size or L2_BYTES_FALLBACK

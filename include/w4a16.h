@@ -317,6 +317,28 @@ int w4a16_select_path(int M, int N, int K, int G, int sym, int dtype);
  * or a NULL pointer. */
 int w4a16_debug_prefill_plan(int M, int N, int K, int dense, int sm_count, const int *clusters, int *out);
 
+/* Profiling hook: a per-CTA timeline of the decode kernel.  trace_buf
+ * (device memory, 8-byte aligned, caller-owned, 4 x 512 x 8 uint64 =
+ * 131072 bytes, zeroed by the caller) receives, for every CTA c < 512 of a
+ * decode launch whose (N, K) is pair i of nk (8 ints: up to four (N, K)
+ * pairs; unused pairs 0), at [i][c][e] the %globaltimer value in ns of event
+ * e: 0 entry, 1 grid-dependency wait returned, 2 x staged, 3 first weight
+ * stage ready, 4 loop end, 5 cluster partials gathered (cluster rank 0
+ * only), 6 exit; [i][c][7] is the CTA's cluster rank.  The buffer travels
+ * in the launch parameters, so the setting applies to launches made (and
+ * CUDA graphs captured) after this call; a graph captured before it keeps
+ * the setting it was captured with.  Each launch of a traced layer
+ * overwrites its entries (the last one wins); MoE launches are not traced.
+ * trace_buf = NULL turns the trace off (the default).  The buffer must
+ * outlive every launch and graph that writes it.  Host state, not
+ * thread-safe against concurrent launches.  The stamps exist only in the
+ * trace build of the library (compiled with W4A16_DECODE_TRACE defined,
+ * libw4a16_trace.so); the default build's decode kernel has none, and there
+ * any non-NULL trace_buf returns W4A16_ERR_ARG.  Returns W4A16_OK,
+ * W4A16_ERR_ARG (nk NULL, a misaligned buffer, or a buffer given to the
+ * default build) or W4A16_ERR_DEVICE. */
+int w4a16_debug_decode_trace(unsigned long long *trace_buf_or_null, const int *nk);
+
 /* The decode GEMM (M <= 8) without any device allocation, ever.  The pages
  * have no counterpart of this entry point: it is a library addition for
  * callers that must not allocate device memory after start-up (an engine

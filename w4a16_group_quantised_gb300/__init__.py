@@ -17,6 +17,7 @@ from .binding import (  # noqa: F401
     library_path,
     load_library,
     w4a16_clear_device_error,
+    w4a16_debug_decode_trace,
     w4a16_debug_set_config,
     w4a16_dequant_debug,
     w4a16_gemm,

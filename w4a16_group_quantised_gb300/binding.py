@@ -34,11 +34,16 @@ class W4A16Error(RuntimeError):
 
 
 def library_path() -> str:
-    return os.path.join(_HERE, _LIBNAME)
+    """libw4a16.so, or with W4A16_LIBRARY=trace the profiling build
+    libw4a16_trace.so (the decode kernel's timeline stamps compiled in)."""
+    v = os.environ.get("W4A16_LIBRARY", "")
+    if v not in ("", "trace"):
+        raise ValueError(f"W4A16_LIBRARY={v!r}: expected unset or 'trace'")
+    return os.path.join(_HERE, "libw4a16_trace.so" if v == "trace" else _LIBNAME)
 
 
 def load_library():
-    """Load libw4a16.so; raises if it has not been built."""
+    """Load the library (library_path()); raises if it has not been built."""
     global _lib
     with _lock:
         if _lib is not None:
@@ -46,7 +51,8 @@ def load_library():
         path = library_path()
         if not os.path.exists(path):
             raise RuntimeError(
-                f"{path} is missing: build it with w4a16_group_quantised_gb300.build.build()")
+                f"{path} is missing: build it with w4a16_group_quantised_gb300.build.build()"
+                + (" (variant='trace')" if path.endswith("_trace.so") else ""))
         lib = ctypes.CDLL(path)
         P, I, L = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong
         sig = {
@@ -72,6 +78,8 @@ def load_library():
             "w4a16_clear_device_error": [],
             "w4a16_version": [],
             "w4a16_debug_set_config": [I, P, I],
+            "w4a16_debug_prefill_plan": [I, I, I, I, I, P, P],
+            "w4a16_debug_decode_trace": [P, P],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -445,6 +453,34 @@ def w4a16_debug_set_config(which: int, vals=None) -> None:
         arr = (ctypes.c_int * len(vals))(*[int(v) for v in vals])
         rc = lib.w4a16_debug_set_config(which, arr, len(vals))
     _check("w4a16_debug_set_config", rc)
+
+
+TRACE_LAYERS, TRACE_CTAS, TRACE_EVENTS = 4, 512, 8
+
+
+def w4a16_debug_decode_trace(shapes=None):
+    """Profiling hook (see include/w4a16.h), in the trace build of the
+    library only (W4A16_LIBRARY=trace): with shapes = up to four (N, K)
+    pairs, every later decode launch of such a layer writes its per-CTA
+    timeline into a device buffer, which is returned ([4, 512, 8] int64:
+    %globaltimer ns of entry, release, x staged, first stage, loop end,
+    gather, exit, then the cluster rank; zero where no CTA wrote).
+    shapes=None turns the trace off and returns None.  The default library
+    raises W4A16Error (W4A16_ERR_ARG) for a non-None shapes."""
+    import torch
+    lib = load_library()
+    if shapes is None:
+        _check("w4a16_debug_decode_trace", lib.w4a16_debug_decode_trace(None, None))
+        return None
+    if not 1 <= len(shapes) <= TRACE_LAYERS:
+        raise ValueError("w4a16_debug_decode_trace: one to four (N, K) pairs")
+    nk = [0] * (2 * TRACE_LAYERS)
+    for i, (n, k) in enumerate(shapes):
+        nk[2 * i], nk[2 * i + 1] = int(n), int(k)
+    buf = torch.zeros((TRACE_LAYERS, TRACE_CTAS, TRACE_EVENTS), dtype=torch.int64, device="cuda")
+    arr = (ctypes.c_int * len(nk))(*nk)
+    _check("w4a16_debug_decode_trace", lib.w4a16_debug_decode_trace(ctypes.c_void_p(buf.data_ptr()), arr))
+    return buf
 
 
 def w4a16_last_device_error() -> int:

@@ -716,6 +716,17 @@ int w4a16_select_path(int M, int N, int K, int G, int sym, int dtype) {
     return select_path_impl(M, N, K, G, sym != 0, dtype);
 }
 
+int w4a16_debug_decode_trace(unsigned long long *trace_buf, const int *nk) {
+    const DeviceInfo *dev = nullptr;
+    int rc = get_device(&dev);
+    if (rc != W4A16_OK) return rc;
+    if (trace_buf != nullptr && (nk == nullptr || (reinterpret_cast<uintptr_t>(trace_buf) & 7u) != 0))
+        return W4A16_ERR_ARG;
+    // cudaErrorNotSupported: a buffer given to a library built without the trace
+    return decode_trace_install(trace_buf, trace_buf != nullptr ? nk : nullptr) == cudaSuccess ? W4A16_OK
+                                                                                               : W4A16_ERR_ARG;
+}
+
 int w4a16_debug_prefill_plan(int M, int N, int K, int dense, int sm_count, const int *clusters, int *out) {
     if (M <= 0 || N <= 0 || K <= 0 || N % 8 != 0 || K % 8 != 0 || sm_count <= 0 || clusters == nullptr ||
         out == nullptr)

@@ -83,6 +83,9 @@ struct DecodeParams {
     int gmax;        // max groups per CTA slice
     int silu;        // SiLU-and-multiply epilogue: rows are [gate | up], I = N / 2 each
     int hold;        // test hook: issue no weight copies, so the bounded waits run out
+#ifdef W4A16_DECODE_TRACE
+    unsigned long long *trace;   // timeline hook: this launch's [kTraceCtas][kTraceEvents] stamps, or null
+#endif
     // expert mode (expert_ids != null): x [T, K], out [T * topk, N], weights [E * N] rows
     const int *expert_ids;   // [T * topk]
     const float *route_w;    // [T * topk] or null
@@ -131,6 +134,27 @@ __host__ __device__ inline DecodeSmem decode_layout(int R, int NW, int NB, int N
     return L;
 }
 
+// Optional per-CTA timeline, compiled only into the trace build of the
+// library (W4A16_DECODE_TRACE defined; the default build has none of it, so
+// its kernel is unchanged).  The host hands a traced layer's launch (matched
+// by N, K; up to four layers) its slice of the buffer that
+// w4a16_debug_decode_trace installed, in the launch parameters.  Thread 0 of
+// each of the first 512 CTAs writes %globaltimer at entry [0], when the
+// grid-dependency wait returns [1], when x is staged [2], when its first
+// weight stage is ready [3], at the end of its loop [4], when its cluster's
+// partials are gathered [5, rank 0 only] and at exit [6]; [7] holds its
+// cluster rank.
+#ifdef W4A16_DECODE_TRACE
+#define DECODE_STAMP(e) \
+    do {                \
+        if (trace) trace[e] = globaltimer(); \
+    } while (0)
+#else
+#define DECODE_STAMP(e) \
+    do {                \
+    } while (0)
+#endif
+
 template <int DT, bool ASYM, int R, int NB>
 __global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ DecodeMaps maps,
                                                      const DecodeParams p) {
@@ -167,6 +191,13 @@ __global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ 
     }
     const int n_tile0 = silu ? tile * RH : tile * RT;
     const DecodeSmem L = decode_layout(R, NW, NB, NS, M, p.xpitch, gmax, ASYM, S);
+#ifdef W4A16_DECODE_TRACE
+    unsigned long long *trace = (p.trace != nullptr && threadIdx.x == 0 && blockIdx.x < kTraceCtas)
+                                    ? p.trace + (size_t)blockIdx.x * kTraceEvents
+                                    : nullptr;                 // thread 0 of a traced launch only
+    if (trace) trace[7] = (unsigned long long)rank;
+#endif
+    DECODE_STAMP(0);
 
     grid_dependents_launch();
 
@@ -286,6 +317,7 @@ __global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ 
 
         // ---- x slice -> shared memory, permuted; zero for k >= K
         grid_dependency_wait();
+        DECODE_STAMP(1);
         {
             unsigned char *xs = smem + L.x;
             const int nch = nb * 16;                   // 16-byte chunks per row
@@ -306,6 +338,7 @@ __global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ 
             }
         }
         named_barrier_sync(1, (uint32_t)nthr);
+        DECODE_STAMP(2);
 
         // Independent accumulator chains per row block: four for one block per
         // warp, two for two (keeps the register count, and so the CTAs per SM,
@@ -335,6 +368,7 @@ __global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ 
                 ok = false;
                 break;
             }
+            if (step == 0) DECODE_STAMP(3);
             const unsigned char *stage = smem + L.ring + (size_t)s * stage_bytes;
             const int lb0 = step * NB;
 #pragma unroll
@@ -375,6 +409,7 @@ __global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ 
             }
         }
 
+        DECODE_STAMP(4);
         // ---- partial sums -> shared memory: red[row][m]
         if (S == 1) {
 #pragma unroll
@@ -427,6 +462,7 @@ __global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ 
         // (their bytes complete the gather barrier)
         __syncthreads();
         if (S > 1) mbar_wait_cluster_bounded(gbar, 0u, p.status, abort_flag);
+        DECODE_STAMP(5);
         if (!silu) {
             const float rw = p.route_w != nullptr ? p.route_w[slot] : 1.0f;
             for (int i = threadIdx.x; i < RT * M; i += blockDim.x) {
@@ -444,6 +480,7 @@ __global__ void __launch_bounds__(288, 2) decode_kernel(const __grid_constant__ 
             }
         }
     }
+    DECODE_STAMP(6);
 }
 
 // ------------------------------------------------------------------ host side
@@ -665,6 +702,21 @@ static cudaError_t launch_dispatch(int dtype, bool asym, int R, int NB, const De
                 : launch_rnb<1, false>(R, NB, tw, p, c, smem, s, pdl, grid);
 }
 
+#ifdef W4A16_DECODE_TRACE
+// The timeline hook's buffer and traced (N, K) pairs (host side; set by
+// decode_trace_install, read when a launch's parameters are built).
+static unsigned long long *g_trace_buf = nullptr;
+static int g_trace_nk[2 * kTraceLayers] = {};
+
+static unsigned long long *decode_trace_slice(const GemmArgs &a) {
+    if (g_trace_buf == nullptr || a.expert_ids != nullptr) return nullptr;
+    for (int i = 0; i < kTraceLayers; ++i)
+        if (g_trace_nk[2 * i] == a.N && g_trace_nk[2 * i + 1] == a.K)
+            return g_trace_buf + (size_t)i * kTraceCtas * kTraceEvents;
+    return nullptr;
+}
+#endif
+
 cudaError_t launch_decode(const GemmArgs &a, const DecodeCfg &c, const DeviceInfo &dev,
                           cudaStream_t s, bool pdl, bool hold_copies) {
     if (dev.encode_tiled == nullptr) return cudaErrorNotSupported;
@@ -712,6 +764,9 @@ cudaError_t launch_decode(const GemmArgs &a, const DecodeCfg &c, const DeviceInf
     p.bias = (const uint16_t *)a.bias;
     p.silu = a.silu_mul ? 1 : 0;
     p.hold = hold_copies ? 1 : 0;
+#ifdef W4A16_DECODE_TRACE
+    p.trace = decode_trace_slice(a);
+#endif
     p.expert_ids = a.expert_ids;
     p.route_w = a.route_w;
     p.n_experts = a.n_experts;
@@ -739,6 +794,17 @@ cudaError_t launch_decode(const GemmArgs &a, const DecodeCfg &c, const DeviceInf
     const int grid = (int)grid_ll;
     const size_t smem = decode_smem_bytes(c, a.M, a.K, a.G, asym);
     return launch_dispatch(a.dtype, asym, c.R, c.NB, tw, p, c, smem, s, pdl, grid);
+}
+
+cudaError_t decode_trace_install(unsigned long long *buf, const int *nk) {
+#ifdef W4A16_DECODE_TRACE
+    g_trace_buf = buf;
+    for (int i = 0; i < 2 * kTraceLayers; ++i) g_trace_nk[i] = (buf != nullptr && nk != nullptr) ? nk[i] : 0;
+    return cudaSuccess;
+#else
+    (void)nk;
+    return buf == nullptr ? cudaSuccess : cudaErrorNotSupported;   // not compiled into this build
+#endif
 }
 
 }  // namespace w4a16

@@ -53,6 +53,12 @@ struct DecodeCfg {
 // slots > 1: an MoE launch of `slots` expert matrices of N rows each (one token each)
 DecodeCfg decode_pick_cfg(int M, int N, int K, int G, int sym, int dtype, int sm_count, int smem_per_sm,
                           int slots = 1);
+// Decode timeline hook: buf (device, kTraceLayers x kTraceCtas x kTraceEvents
+// uint64) or null to turn it off; nk = (N, K) of up to four traced layers.
+// Only the trace build (W4A16_DECODE_TRACE) records anything; the default
+// build returns cudaErrorNotSupported for a non-null buf.
+constexpr int kTraceLayers = 4, kTraceCtas = 512, kTraceEvents = 8;
+cudaError_t decode_trace_install(unsigned long long *buf, const int *nk);
 bool decode_cfg_valid(const DecodeCfg &c, int M, int K, int G, bool asym);
 size_t decode_smem_bytes(const DecodeCfg &c, int M, int K, int G, bool asym);
 // hold_copies: test hook -- the kernel issues no weight copies, so its bounded
